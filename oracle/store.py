@@ -1,0 +1,172 @@
+"""Oracle for the index-key store: RMSNorm + RoPE + quantise + paged write.
+
+What the store computes ("The Moment of Validation", section "Input
+Knowledge Required to Understand This Message": the fused kernel normalises,
+applies RoPE and stores each index key in one pass; "The Fused Kernel
+Decision", section "The Message": a 64-token paged layout in which a token
+maps to a page and an offset inside it):
+
+  y    = RMSNorm(x) = x / sqrt(mean(x^2) + eps) * gamma       (128 dims)
+  y'   = RoPE(y, pos), dims i and i+64 rotated by pos * theta^(-2i/128)
+  bf16 : store round(y') as 128 bf16 values                   (256 B/token)
+  fp8  : scale = max|y'| / 448, store e4m3(y' / scale) (128 B) and the fp32
+         scale (4 B)                                          (132 B/token)
+
+The bytes are decided by floating point, so the oracle computes them in the
+precision the kernel uses (fp32) with one fixed order of operations, which is
+the definition the stored bytes are compared against:
+
+  * sum of squares: 16 partial sums over consecutive groups of 8 dims,
+    each accumulated in dim order; then the partials are added pairwise,
+    (g, g+8), then (g, g+4), (g, g+2), (g, g+1);
+  * mean = sum * (1/128) (exact); r = 1 / sqrt(mean + eps), each operation
+    rounded to nearest;
+  * y_d = (x_d * r) * gamma_d;
+  * RoPE, with c = cos(pos*f_i), s = sin(pos*f_i), f_i = theta^(-2i/128)
+    evaluated in double by the host C library and rounded once to fp32:
+        y'_i      = y_i * c - y_{i+64} * s
+        y'_{i+64} = y_{i+64} * c + y_i * s
+    every product and sum rounded separately (no fused multiply-add);
+  * fp8: amax = max(max_d |y'_d|, 1e-4); scale = amax / 448;
+    inv = 1 / scale; code_d = e4m3_satfinite(y'_d * inv).
+
+The 1e-4 floor on amax is this library's reading for an all-zero key (the
+pages do not say); it keeps the scale positive, which the scorer relies on.
+
+Cache layouts (per page of 64 tokens):
+  bf16 : [64][128] bf16                         16384 bytes
+  fp8  : [64][128] e4m3, then [64] fp32 scales   8448 bytes
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import formats as F
+
+D = 128
+HALF = 64
+PAGE = 64
+FMT_BF16 = 0
+FMT_FP8 = 1
+PAGE_BYTES = {FMT_BF16: PAGE * D * 2, FMT_FP8: PAGE * D + PAGE * 4}
+TOKEN_BYTES = {FMT_BF16: D * 2, FMT_FP8: D + 4}
+AMAX_FLOOR = np.float32(1e-4)
+
+
+def rope_cos_sin(theta: float, positions: np.ndarray):
+    """fp32 cos/sin of pos * theta^(-2i/128) for i < 64, from double libm."""
+    positions = np.asarray(positions, dtype=np.int64)
+    uniq, inv = np.unique(positions, return_inverse=True)
+    freqs = [math.pow(float(theta), -(2.0 * i) / D) for i in range(HALF)]
+    cu = np.empty((len(uniq), HALF), dtype=np.float32)
+    su = np.empty((len(uniq), HALF), dtype=np.float32)
+    for r, p in enumerate(uniq.tolist()):
+        cu[r] = [math.cos(p * f) for f in freqs]
+        su[r] = [math.sin(p * f) for f in freqs]
+    return cu[inv], su[inv]
+
+
+def rmsnorm_f32(x: np.ndarray, eps: float, gamma: np.ndarray | None = None) -> np.ndarray:
+    """RMSNorm of fp32 rows [T,128] in the fixed fp32 order stated above."""
+    x = np.asarray(x, dtype=np.float32)
+    T = x.shape[0]
+    sq = (x * x).reshape(T, 16, 8)            # exact: x has <= 8 significant bits
+    p = sq[:, :, 0].copy()
+    for j in range(1, 8):
+        p = p + sq[:, :, j]
+    t = p[:, :8] + p[:, 8:]
+    t = t[:, :4] + t[:, 4:]
+    t = t[:, :2] + t[:, 2:]
+    ss = t[:, 0] + t[:, 1]
+    ms = ss * np.float32(1.0 / 128.0)
+    r = np.float32(1.0) / np.sqrt(ms + np.float32(eps))
+    y = x * r[:, None]
+    if gamma is not None:
+        y = y * np.asarray(gamma, dtype=np.float32)[None, :]
+    return y
+
+
+def rope_f32(y: np.ndarray, c: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Half-split RoPE in fp32, each operation rounded separately."""
+    a = y[:, :HALF]
+    b = y[:, HALF:]
+    out = np.empty_like(y)
+    out[:, :HALF] = a * c - b * s
+    out[:, HALF:] = b * c + a * s
+    return out
+
+
+def normalize_rotate(k_raw_bits: np.ndarray, pos: np.ndarray, theta: float, eps: float,
+                     gamma_bits: np.ndarray | None = None) -> np.ndarray:
+    """fp32 y' for bf16 raw keys [T,128] at positions pos [T]."""
+    x = F.bf16_to_f64(k_raw_bits).astype(np.float32)
+    gamma = None if gamma_bits is None else F.bf16_to_f64(gamma_bits).astype(np.float32)
+    y = rmsnorm_f32(x, eps, gamma)
+    c, s = rope_cos_sin(theta, pos)
+    return rope_f32(y, c, s)
+
+
+def quantize_fp8(yr: np.ndarray):
+    """Per-token amax scale and e4m3 codes of fp32 rows."""
+    amax = np.maximum(np.max(np.abs(yr), axis=1), AMAX_FLOOR).astype(np.float32)
+    scale = (amax / np.float32(F.E4M3_MAX)).astype(np.float32)
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    codes = F.f32_to_e4m3_satfinite(yr * inv[:, None])
+    return codes, scale
+
+
+def new_cache(num_pages: int, fmt: int) -> np.ndarray:
+    return np.zeros(num_pages * PAGE_BYTES[fmt], dtype=np.uint8)
+
+
+def slots(pos: np.ndarray, seq: np.ndarray, page_table: np.ndarray, num_pages: int):
+    """(page, offset) of each token: page_table[seq][pos // 64], pos % 64."""
+    pos = np.asarray(pos, dtype=np.int64)
+    seq = np.asarray(seq, dtype=np.int64)
+    page = np.asarray(page_table, dtype=np.int64)[seq, pos // PAGE]
+    if np.any((page < 0) | (page >= num_pages)):
+        raise ValueError("page id out of range")
+    return page, pos % PAGE
+
+
+def store(cache: np.ndarray, fmt: int, k_raw_bits, pos, seq, page_table, num_pages: int,
+          theta: float = 10000.0, eps: float = 1e-6, gamma_bits=None) -> None:
+    """Write the tokens' index keys into the byte image of the paged cache."""
+    if len(pos) == 0:
+        return
+    yr = normalize_rotate(k_raw_bits, pos, theta, eps, gamma_bits)
+    page, off = slots(pos, seq, page_table, num_pages)
+    pb = PAGE_BYTES[fmt]
+    if fmt == FMT_BF16:
+        b = F.f32_to_bf16(yr).view(np.uint8).reshape(-1, 2 * D)
+        base = page * pb + off * 2 * D
+        idx = base[:, None] + np.arange(2 * D)[None, :]
+        cache[idx] = b
+    else:
+        codes, scale = quantize_fp8(yr)
+        base = page * pb + off * D
+        cache[base[:, None] + np.arange(D)[None, :]] = codes
+        sb = page * pb + PAGE * D + off * 4
+        cache[sb[:, None] + np.arange(4)[None, :]] = scale.astype("<f4").view(np.uint8).reshape(-1, 4)
+
+
+def read_keys(cache: np.ndarray, fmt: int, page_table_row: np.ndarray, n: int) -> np.ndarray:
+    """Exact float64 values of the stored keys at positions 0..n-1 of one
+    sequence (fp8: e4m3 value times the token's scale, exact in double)."""
+    if n == 0:
+        return np.zeros((0, D))
+    pos = np.arange(n, dtype=np.int64)
+    page = np.asarray(page_table_row, dtype=np.int64)[pos // PAGE]
+    off = pos % PAGE
+    pb = PAGE_BYTES[fmt]
+    if fmt == FMT_BF16:
+        base = page * pb + off * 2 * D
+        raw = cache[base[:, None] + np.arange(2 * D)[None, :]]
+        return F.bf16_to_f64(raw.copy().view(np.uint16))
+    base = page * pb + off * D
+    codes = cache[base[:, None] + np.arange(D)[None, :]]
+    sb = page * pb + PAGE * D + off * 4
+    scale = cache[sb[:, None] + np.arange(4)[None, :]].copy().view("<f4").reshape(-1).astype(np.float64)
+    return F.e4m3_to_f64(codes) * scale[:, None]

@@ -1,0 +1,210 @@
+"""Pins for the oracle's store (RMSNorm + RoPE + quantise + paged write),
+against closed forms, hand-computed examples, an independent float64
+restatement (complex-number form of the rotation) and the fp8 error bound."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import formats as F
+from oracle import store as S
+from synth import inputs as I
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+ULP32 = 2.0 ** -23
+
+
+def _bf16(vals):
+    return F.f32_to_bf16(np.asarray(vals, dtype=np.float32))
+
+
+def test_layout_matches_pages():
+    g = json.load(open(os.path.join(GOLD, "layout.json")))
+    assert S.TOKEN_BYTES[S.FMT_FP8] == g["fp8_bytes_per_token"]
+    assert S.TOKEN_BYTES[S.FMT_BF16] == g["bf16_bytes_per_token"]
+    assert S.PAGE == g["page_size"] and S.D == g["head_dim"]
+    assert S.PAGE_BYTES[S.FMT_BF16] == 2 * g["bf16_page_elements"]
+    assert S.PAGE_BYTES[S.FMT_FP8] == g["page_size"] * g["fp8_bytes_per_token"]
+
+
+@pytest.mark.parametrize("c", [1.0, -0.5, 3.25, 1e-3, 100.0])
+def test_rmsnorm_constant_vector(c):
+    x = F.bf16_to_f64(_bf16(np.full((1, 128), c))).astype(np.float32)
+    cv = float(x[0, 0])
+    y = S.rmsnorm_f32(x, 1e-6)
+    want = cv / math.sqrt(cv * cv + float(np.float32(1e-6)))
+    assert np.allclose(y, want, rtol=4 * ULP32, atol=0)
+
+
+@pytest.mark.parametrize("j,a", [(0, 1.0), (77, -2.5), (127, 0.125)])
+def test_rmsnorm_one_hot(j, a):
+    x = np.zeros((1, 128), np.float32)
+    x[0, j] = a
+    y = S.rmsnorm_f32(x, 1e-6)
+    want = a / math.sqrt(a * a / 128 + float(np.float32(1e-6)))
+    assert abs(y[0, j] - want) <= 4 * ULP32 * abs(want)
+    assert np.count_nonzero(y) == 1
+    # |y| -> sqrt(128) when a*a/128 >> eps
+    if abs(a) >= 1:
+        assert abs(abs(y[0, j]) - math.sqrt(128)) < 1e-3 * math.sqrt(128)
+
+
+def test_rmsnorm_gamma_multiplies():
+    rng = np.random.default_rng(0)
+    x = F.bf16_to_f64(_bf16(rng.standard_normal((4, 128)))).astype(np.float32)
+    g = F.bf16_to_f64(_bf16(rng.uniform(0.5, 2, 128))).astype(np.float32)
+    y1 = S.rmsnorm_f32(x, 1e-6)
+    y2 = S.rmsnorm_f32(x, 1e-6, g)
+    assert np.array_equal(y2, y1 * g[None, :])
+
+
+def test_rope_position_zero_is_identity():
+    rng = np.random.default_rng(1)
+    kb = _bf16(rng.standard_normal((8, 128)))
+    x = F.bf16_to_f64(kb).astype(np.float32)
+    y = S.rmsnorm_f32(x, 1e-6)
+    yr = S.normalize_rotate(kb, np.zeros(8, np.int32), 10000.0, 1e-6)
+    assert np.array_equal(y, yr)
+
+
+@pytest.mark.parametrize("i,pos", [(0, 1), (1, 5), (63, 1000), (10, 131071)])
+def test_rope_half_split_pairing_hand_example(i, pos):
+    # one-hot at dim i rotates into dims i (cos) and i+64 (sin); nothing else moves
+    x = np.zeros((1, 128), np.float32)
+    x[0, i] = 1.0
+    yr = S.normalize_rotate(_bf16(x), np.array([pos]), 10000.0, 1e-6)
+    a = 1.0 / math.sqrt(1.0 / 128 + float(np.float32(1e-6)))
+    ang = pos * 10000.0 ** (-2.0 * i / 128)
+    nz = set(np.nonzero(yr[0])[0].tolist())
+    assert nz <= {i, i + 64}
+    assert abs(yr[0, i] - a * math.cos(ang)) <= 8 * ULP32 * a
+    assert abs(yr[0, i + 64] - a * math.sin(ang)) <= 8 * ULP32 * a
+
+
+def test_rope_matches_complex_rotation_fp64():
+    rng = np.random.default_rng(2)
+    T = 256
+    kb = _bf16(rng.standard_normal((T, 128)))
+    pos = rng.integers(0, 200000, T)
+    yr = S.normalize_rotate(kb, pos, 10000.0, 1e-6).astype(np.float64)
+    x = F.bf16_to_f64(kb)
+    y = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + float(np.float32(1e-6)))
+    f = 10000.0 ** (-np.arange(64) * 2.0 / 128)
+    z = (y[:, :64] + 1j * y[:, 64:]) * np.exp(1j * pos[:, None] * f[None, :])
+    want = np.concatenate([z.real, z.imag], axis=1)
+    err = np.abs(yr - want).max(axis=1) / np.abs(want).max(axis=1)
+    assert err.max() < 1e-6
+
+
+def test_rope_relative_position_property():
+    # <RoPE_m(a), RoPE_n(b)> depends only on m - n
+    rng = np.random.default_rng(3)
+    kb = _bf16(rng.standard_normal((2, 128)))
+    def dot(m, n):
+        ya = S.normalize_rotate(kb[:1], np.array([m]), 10000.0, 1e-6).astype(np.float64)
+        yb = S.normalize_rotate(kb[1:], np.array([n]), 10000.0, 1e-6).astype(np.float64)
+        return float(ya[0] @ yb[0])
+    base = dot(10, 3)
+    for t in (1, 77, 5000, 100000):
+        assert abs(dot(10 + t, 3 + t) - base) < 1e-4 * 128
+    assert abs(dot(10, 3) - dot(3, 10)) > 1e-3  # not symmetric in general
+
+
+def test_store_bf16_matches_fp64_definition():
+    # independent float64 restatement; bytes must equal RNE(fp64 value)
+    # except where the fp64 value sits within 1e-5 relative of a bf16 tie
+    rng = np.random.default_rng(4)
+    T = 2000
+    kb = _bf16(rng.standard_normal((T, 128)) * np.exp(rng.uniform(-3, 3, (T, 1))))
+    pos = rng.integers(0, 70000, T)
+    got = F.f32_to_bf16(S.normalize_rotate(kb, pos, 10000.0, 1e-6))
+    x = F.bf16_to_f64(kb)
+    y = x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + float(np.float32(1e-6)))
+    f = np.array([math.pow(10000.0, -(2.0 * i) / 128) for i in range(64)])
+    z = (y[:, :64] + 1j * y[:, 64:]) * np.exp(1j * pos[:, None] * f[None, :])
+    want64 = np.concatenate([z.real, z.imag], axis=1)
+    # bytes must equal bf16(fp64 value) except where the fp64 value lies within
+    # the fp32 evaluation error (a few 2^-24 of the token's largest element)
+    # of a bf16 rounding midpoint; there the two neighbours are both valid
+    ref = F.f32_to_bf16(want64.astype(np.float32))
+    mism = got != ref
+    assert mism.mean() < 2e-3, mism.mean()
+    # a mismatch is a valid rounding of a value within the fp32 evaluation
+    # error of the fp64 value: |bf16 - w| <= half a bf16 step of |w| + 2^-21 * rowmax
+    gv = F.bf16_to_f64(got)
+    rowmax = np.abs(want64).max(axis=1, keepdims=True) * np.ones_like(want64)
+    _, ex = np.frexp(np.abs(want64))
+    half_step = np.ldexp(1.0, (ex - 1 - 8).astype(np.int32))
+    assert np.all(np.abs(gv - want64)[mism] <= half_step[mism] + 2.0 ** -21 * rowmax[mism])
+
+
+def test_fp8_roundtrip_bound_and_amax_code():
+    rng = np.random.default_rng(5)
+    T = 3000
+    kb = _bf16(rng.standard_normal((T, 128)) * np.exp(rng.uniform(-5, 5, (T, 128))))
+    yr = S.normalize_rotate(kb, rng.integers(0, 5000, T), 10000.0, 1e-6)
+    codes, scale = S.quantize_fp8(yr)
+    deq = F.e4m3_to_f64(codes) * scale[:, None].astype(np.float64)
+    y = yr.astype(np.float64)
+    bound = np.maximum(2.0 ** -4 * np.abs(y), 2.0 ** -10 * scale[:, None])
+    assert np.all(np.abs(y - deq) <= bound * (1 + 1e-6))
+    # the largest element of each token maps to +-448
+    am = np.argmax(np.abs(y), axis=1)
+    top = codes[np.arange(T), am]
+    assert np.all((top & 0x7F) == 0x7E)
+    assert np.allclose(scale, np.abs(y).max(axis=1) / 448, rtol=2 * ULP32)
+
+
+def test_fp8_zero_token():
+    yr = np.zeros((1, 128), np.float32)
+    codes, scale = S.quantize_fp8(yr)
+    assert np.all(codes == 0)
+    assert scale[0] == np.float32(np.float32(1e-4) / np.float32(448))
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+def test_paged_store_placement_and_permutation(fmt):
+    wl = I.make_workload("t", [300, 130], [1, 1], [300, 130], True, 512, seed=7, wid=9)
+    cache = S.new_cache(wl.num_pages, fmt)
+    S.store(cache, fmt, wl.new_k, wl.new_pos, wl.new_seq, wl.page_table, wl.num_pages)
+    # same tokens through an identity page table read back identically
+    ident = np.full_like(wl.page_table, -1)
+    c = 0
+    for b, L in enumerate(wl.seq_lens):
+        n = (int(L) + 63) // 64
+        ident[b, :n] = np.arange(c, c + n)
+        c += n
+    cache2 = S.new_cache(wl.num_pages, fmt)
+    S.store(cache2, fmt, wl.new_k, wl.new_pos, wl.new_seq, ident, wl.num_pages)
+    for b, L in enumerate(wl.seq_lens):
+        k1 = S.read_keys(cache, fmt, wl.page_table[b], int(L))
+        k2 = S.read_keys(cache2, fmt, ident[b], int(L))
+        assert np.array_equal(k1, k2)
+    # token bytes land at page*page_bytes + off*token_bytes (bf16: 256 B rows)
+    t = 5
+    b, p = int(wl.new_seq[t]), int(wl.new_pos[t])
+    page = int(wl.page_table[b, p // 64])
+    yr = S.normalize_rotate(wl.new_k[t:t + 1], wl.new_pos[t:t + 1], 10000.0, 1e-6)
+    if fmt == S.FMT_BF16:
+        off = page * 16384 + (p % 64) * 256
+        assert np.array_equal(cache[off:off + 256].view(np.uint16), F.f32_to_bf16(yr)[0])
+    else:
+        codes, sc = S.quantize_fp8(yr)
+        off = page * 8448 + (p % 64) * 128
+        assert np.array_equal(cache[off:off + 128], codes[0])
+        so = page * 8448 + 8192 + (p % 64) * 4
+        assert cache[so:so + 4].view("<f4")[0] == sc[0]
+    # the last page of sequence 1 (130 tokens -> 3 pages, 2 slots used) keeps zeros
+    last = int(wl.page_table[1, 2])
+    tb = S.TOKEN_BYTES[fmt] if fmt == S.FMT_BF16 else 128
+    base = last * S.PAGE_BYTES[fmt]
+    assert np.all(cache[base + 2 * tb: base + 64 * tb] == 0)
+
+
+def test_bad_page_id_rejected():
+    pt = np.array([[0, 5]], np.int32)
+    cache = S.new_cache(2, S.FMT_BF16)
+    with pytest.raises(ValueError):
+        S.store(cache, S.FMT_BF16, _bf16(np.ones((1, 128))), np.array([64]), np.array([0]), pt, 2)
