@@ -1,0 +1,174 @@
+// C ABI of libdsaidx: context set-up (RoPE table, gamma, status word),
+// argument validation, and dispatch to the store and top-k launchers.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "internal.cuh"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaStream_t as_stream(dsa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_str(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_DEVICE_BOUNDS: return "device saw an out-of-range page id, position or sequence";
+    case DSA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case DSA_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+size_t dsa_cache_page_bytes(dsa_fmt fmt) {
+  if (fmt == DSA_FMT_BF16) return DSA_PAGE_SIZE * DSA_HEAD_DIM * 2;
+  if (fmt == DSA_FMT_FP8) return DSA_PAGE_SIZE * DSA_HEAD_DIM + DSA_PAGE_SIZE * 4;
+  return 0;
+}
+
+dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_t max_pos,
+                          const uint16_t* gamma_bf16) {
+  if (!out || !(rope_theta > 0.f) || !(rms_eps >= 0.f) || max_pos <= 0) return DSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (major != 10 || minor != 3) return DSA_ERR_UNSUPPORTED;
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult qres;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &qres) != cudaSuccess ||
+      qres != cudaDriverEntryPointSuccess || !fn)
+    return DSA_ERR_CUDA;
+
+  // RoPE table: angle pos * theta^(-2i/128) in double, cos/sin rounded once to fp32
+  const size_t n = static_cast<size_t>(max_pos) * 64;
+  std::vector<float2> tab(n);
+  double freq[64];
+  for (int i = 0; i < 64; ++i) freq[i] = std::pow(static_cast<double>(rope_theta), -(2.0 * i) / 128.0);
+  for (int32_t p = 0; p < max_pos; ++p)
+    for (int i = 0; i < 64; ++i) {
+      const double a = static_cast<double>(p) * freq[i];
+      tab[static_cast<size_t>(p) * 64 + i] =
+          make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+    }
+  float g[128];
+  for (int d = 0; d < 128; ++d) {
+    if (gamma_bf16) {
+      const uint32_t b = static_cast<uint32_t>(gamma_bf16[d]) << 16;
+      std::memcpy(&g[d], &b, 4);
+    } else {
+      g[d] = 1.0f;
+    }
+  }
+
+  dsa_ctx* c = static_cast<dsa_ctx*>(std::calloc(1, sizeof(dsa_ctx)));
+  if (!c) return DSA_ERR_CUDA;
+  c->device = dev;
+  c->num_sms = sms;
+  c->theta = rope_theta;
+  c->eps = rms_eps;
+  c->max_pos = max_pos;
+  c->encode_tiled = fn;
+  bool okk = cudaMalloc(&c->rope, n * sizeof(float2)) == cudaSuccess &&
+             cudaMalloc(&c->gamma, 128 * sizeof(float)) == cudaSuccess &&
+             cudaMalloc(&c->status, sizeof(unsigned int)) == cudaSuccess &&
+             cudaMemcpy(c->rope, tab.data(), n * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
+             cudaMemcpy(c->gamma, g, sizeof(g), cudaMemcpyHostToDevice) == cudaSuccess &&
+             cudaMemset(c->status, 0, sizeof(unsigned int)) == cudaSuccess;
+  if (!okk) {
+    cudaFree(c->rope);
+    cudaFree(c->gamma);
+    cudaFree(c->status);
+    std::free(c);
+    return DSA_ERR_CUDA;
+  }
+  *out = c;
+  return DSA_OK;
+}
+
+dsa_status dsa_ctx_destroy(dsa_ctx* ctx) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  cudaFree(ctx->rope);
+  cudaFree(ctx->gamma);
+  cudaFree(ctx->status);
+  std::free(ctx);
+  return DSA_OK;
+}
+
+dsa_status dsa_get_device_status(dsa_ctx* ctx, dsa_stream_t stream) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  unsigned int w = 0;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpy(&w, ctx->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ctx->status, 0, sizeof(w)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (w & DSA_DEV_BOUNDS) return DSA_ERR_DEVICE_BOUNDS;
+  if (w & DSA_DEV_TIMEOUT) return DSA_ERR_TIMEOUT;
+  return DSA_OK;
+}
+
+dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_pos,
+                           const int32_t* seq_id, const int32_t* page_table, int32_t T,
+                           int32_t B, int32_t max_pages, void* cache, int32_t num_pages,
+                           dsa_fmt fmt, dsa_stream_t stream) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return DSA_ERR_UNSUPPORTED;
+  if (T < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
+  if (T == 0) return DSA_OK;
+  if (!k_raw || !rope_pos || !seq_id || !page_table || !cache) return DSA_ERR_INVALID_ARG;
+  if (!aligned(k_raw, 16) || !aligned(cache, 256) || !aligned(rope_pos, 4) || !aligned(seq_id, 4) ||
+      !aligned(page_table, 4))
+    return DSA_ERR_INVALID_ARG;
+  return dsa::launch_store(ctx, k_raw, rope_pos, seq_id, page_table, T, B, max_pages, cache,
+                           num_pages, fmt, as_stream(stream));
+}
+
+size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k,
+                                     dsa_fmt fmt) {
+  if (!ctx || Tq < 0 || B <= 0 || (k != 512 && k != 1024)) return 0;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return 0;
+  return dsa::topk_workspace(ctx, Tq, B, k, fmt);
+}
+
+dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
+                          int32_t num_pages, dsa_fmt fmt, const int32_t* page_table,
+                          int32_t max_pages, const int32_t* seq_lens, const int32_t* cu_q,
+                          int32_t B, int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
+                          float* out_score, void* workspace, size_t ws_bytes,
+                          dsa_stream_t stream) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return DSA_ERR_UNSUPPORTED;
+  if (k != 512 && k != 1024) return DSA_ERR_UNSUPPORTED;
+  if (Tq < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_pages) * 64 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
+  if (Tq == 0) return DSA_OK;
+  if (!q || !head_w || !cache || !page_table || !seq_lens || !cu_q || !out_idx || !out_score ||
+      !workspace)
+    return DSA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(workspace, 256) || !aligned(head_w, 4) ||
+      !aligned(out_idx, 4) || !aligned(out_score, 4))
+    return DSA_ERR_INVALID_ARG;
+  if (ws_bytes < dsa::topk_workspace(ctx, Tq, B, k, fmt)) return DSA_ERR_WORKSPACE;
+  return dsa::launch_topk(ctx, q, head_w, cache, num_pages, fmt, page_table, max_pages, seq_lens,
+                          cu_q, B, Tq, causal ? 1 : 0, k, out_idx, out_score, workspace, ws_bytes,
+                          as_stream(stream));
+}
+
+}  // extern "C"

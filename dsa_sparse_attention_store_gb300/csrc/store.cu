@@ -1,0 +1,161 @@
+// Index-key store kernel: RMSNorm + RoPE + (e4m3 with a per-token scale |
+// bf16) written into a 64-token paged cache.
+//
+// What it computes follows "The Moment of Validation: Diagnosing an OOM Crash
+// in the bf16 Index-K Fix for DeepSeek V4 Sparse Attention" (section "Input
+// Knowledge Required to Understand This Message": normalisation, RoPE and
+// the store fused in one kernel; 132 B/token fp8, 256 B/token bf16) and "The
+// Fused Kernel Decision" (section "The Message": 64-token pages, a token goes
+// to a page and an offset, a bf16 page is [64*128]).
+//
+// Mapping: one token per half-warp. Lane l (0..15) owns dims 8l..8l+7 and
+// moves them with one 16-byte load and one 16-byte (bf16) or 8-byte (fp8)
+// store, so a warp reads 512 contiguous bytes per instruction. The sum of
+// squares is 8 sequential fused multiply-adds per lane (exact products of
+// bf16 inputs) followed by a xor butterfly over the half-warp (8, 4, 2, 1):
+// this order is the store's definition, which is what makes the bytes
+// reproducible. RoPE pairs dim i (lane l < 8) with dim i+64 (lane l+8), one
+// shuffle. Every fp32 step uses the round-to-nearest intrinsics so no
+// multiply-add is contracted.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kPage = 64;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int FMT>
+__global__ void __launch_bounds__(256) store_kernel(
+    const uint4* __restrict__ k_raw, const int32_t* __restrict__ rope_pos,
+    const int32_t* __restrict__ seq_id, const int32_t* __restrict__ page_table, int T, int B,
+    int max_pages, uint8_t* __restrict__ cache, int num_pages, const float2* __restrict__ rope,
+    int max_pos, const float* __restrict__ gamma, float eps, unsigned int* status) {
+  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const int l = threadIdx.x & 15;
+  const bool live = tok < T;
+
+  int pos = 0, page = -1;
+  bool ok = false;
+  if (live) {
+    pos = rope_pos[tok];
+    const int s = seq_id[tok];
+    ok = s >= 0 && s < B && pos >= 0 && pos < max_pos && pos < max_pages * kPage;
+    if (ok) {
+      page = page_table[static_cast<long long>(s) * max_pages + pos / kPage];
+      ok = page >= 0 && page < num_pages;
+    }
+    if (!ok && l == 0) atomicOr(status, DSA_DEV_BOUNDS);
+  }
+
+  uint4 raw = make_uint4(0, 0, 0, 0);
+  if (ok) raw = k_raw[static_cast<long long>(tok) * 16 + l];
+  float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+
+  // sum of squares: sequential in dim order within the lane, then a butterfly
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ss = __fmaf_rn(x[e], x[e], ss);
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
+  const float ms = __fmul_rn(ss, 0.0078125f);
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], r), gamma[8 * l + e]);
+
+  // RoPE, dims i and i+64 (lanes l and l^8)
+  float py[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) py[e] = __shfl_xor_sync(0xffffffffu, y[e], 8);
+  const float4* cs4 =
+      reinterpret_cast<const float4*>(rope + static_cast<long long>(ok ? pos : 0) * 64 + 8 * (l & 7));
+  float c[8], s[8];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const float4 t = ok ? __ldg(cs4 + v) : make_float4(1.f, 0.f, 1.f, 0.f);
+    c[2 * v] = t.x;
+    s[2 * v] = t.y;
+    c[2 * v + 1] = t.z;
+    s[2 * v + 1] = t.w;
+  }
+  float o[8];
+  if (l < 8) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __fsub_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], s[e]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], s[e]));
+  }
+
+  const int off = pos & (kPage - 1);
+  if constexpr (FMT == DSA_FMT_BF16) {
+    if (ok) {
+      uint32_t w[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const __nv_bfloat162 p = __floats2bfloat162_rn(o[2 * v], o[2 * v + 1]);
+        w[v] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(cache + static_cast<long long>(page) * (kPage * kD * 2) +
+                                            off * (kD * 2)) + l;
+      *dst = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(o[e]));
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    amax = fmaxf(amax, 1e-4f);
+    const float scale = __fdiv_rn(amax, 448.0f);
+    const float inv = __fdiv_rn(1.0f, scale);
+    if (ok) {
+      uint32_t w[2];
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(o[4 * v], inv), __fmul_rn(o[4 * v + 1], inv)), __NV_SATFINITE,
+            __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fmul_rn(o[4 * v + 2], inv), __fmul_rn(o[4 * v + 3], inv)),
+            __NV_SATFINITE, __NV_E4M3);
+        w[v] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+      uint8_t* pg = cache + static_cast<long long>(page) * (kPage * kD + kPage * 4);
+      *reinterpret_cast<uint2*>(pg + off * kD + 8 * l) = make_uint2(w[0], w[1]);
+      if (l == 0) *reinterpret_cast<float*>(pg + kPage * kD + off * 4) = scale;
+    }
+  }
+}
+
+}  // namespace
+
+dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, const int32_t* seq,
+                        const int32_t* page_table, int32_t T, int32_t B, int32_t max_pages,
+                        void* cache, int32_t num_pages, dsa_fmt fmt, cudaStream_t stream) {
+  if (T == 0) return DSA_OK;
+  const long long threads = static_cast<long long>(T) * 16;
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  if (fmt == DSA_FMT_BF16)
+    store_kernel<DSA_FMT_BF16><<<blocks, 256, 0, stream>>>(
+        static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B, max_pages,
+        static_cast<uint8_t*>(cache), num_pages, ctx->rope, ctx->max_pos, ctx->gamma, ctx->eps,
+        ctx->status);
+  else
+    store_kernel<DSA_FMT_FP8><<<blocks, 256, 0, stream>>>(
+        static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B, max_pages,
+        static_cast<uint8_t*>(cache), num_pages, ctx->rope, ctx->max_pos, ctx->gamma, ctx->eps,
+        ctx->status);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

@@ -1,0 +1,1091 @@
+// Score + top-k selection of the DSA indexer on sm_103a.
+//
+// What is computed ("The Crash That Changed Direction", sections "The
+// Experiment: Why fp32?" and "Assumptions Made and Broken"): every query's
+// 64 index heads are multiplied against all cached index keys (a batched
+// matrix product), each head's dot product goes through a ReLU, the heads are
+// combined with per-head weights into one score per key, keys after the
+// query's position are masked, and the top-k positions (k = 512 or 1024) are
+// kept. Fp8 keys are up-converted exactly before the product.
+//
+// Why it streams ("When the Fused Kernel Isn't Enough", section "The
+// Message: Validation and Discovery"): materialising the [q_len x ctx]
+// logits ran out of memory at 22K tokens. Here every score lives only in
+// registers; key tiles stream through a per-query running top-k in shared
+// memory. Scratch is the schedule, at most two partial top-k lists per CTA
+// (when a query tile's context is split across CTAs) and, for fp8 caches,
+// the queries converted for the tensor cores.
+//
+// Kernels, in launch order:
+//   plan    one CTA: query tiles (QT queries of one sequence) and a prefix sum
+//           of their key-tile counts, so CTAs can split the total work evenly.
+//   qprep   fp8 caches only: q -> f16 with a power-of-two scale per (query,
+//           head) so the largest magnitude lands in [2^14, 2^15); the scale's
+//           inverse is folded into the head weight (exact).
+//   score   persistent, one CTA per SM, warp-specialised:
+//             warp 0      producer: page-table lookups, TMA of 64-token pages
+//             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
+//                         x K=128 into one of two TMEM accumulators
+//             4*NG warps  epilogue: tcgen05.ld, ReLU, head-weighted sum, mask,
+//                         threshold filter into the running top-k
+//             4 warps     (fp8) e4m3 -> f16 conversion of staged key tiles
+//           Keys sit on the MMA's M dimension so each epilogue thread owns one
+//           key (one TMEM lane) and reduces over heads in its own registers.
+//   sort    one warp per output row: bitonic sort by (score desc, pos asc).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kH = 64;
+constexpr int kD = 128;
+constexpr int kTile = 128;  // keys per MMA tile = 2 pages
+constexpr int kPageBytesBf16 = 64 * 128 * 2;
+constexpr int kPageBytesFp8 = 64 * 128 + 64 * 4;
+
+struct PlanHdr {
+  int qtot;
+  int pad;
+  long long total;
+};
+
+struct WsLayout {
+  size_t hdr, seq_qoff, meta, prefix, counters, partials, qh, wq, total;
+  int QT, G, qtmax, NG;
+};
+
+inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline int pick_qt(int Tq, int B) { return (Tq >= 2 * B && Tq >= 4) ? 4 : 1; }
+
+WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
+  WsLayout L{};
+  L.QT = pick_qt(Tq, B);
+  L.NG = L.QT == 4 ? 2 : 1;
+  L.G = num_sms;
+  L.qtmax = (Tq + L.QT - 1) / L.QT + B;
+  size_t o = 0;
+  L.hdr = o;
+  o += 256;
+  L.seq_qoff = o;
+  o = up256(o + static_cast<size_t>(B + 1) * 4);
+  L.meta = o;
+  o = up256(o + static_cast<size_t>(L.qtmax) * 16);
+  L.prefix = o;
+  o = up256(o + static_cast<size_t>(L.qtmax + 1) * 8);
+  L.counters = o;
+  o = up256(o + static_cast<size_t>(L.qtmax) * L.NG * 4);
+  L.partials = o;
+  o = up256(o + static_cast<size_t>(2) * L.G * L.QT * k * 8);
+  if (fmt == DSA_FMT_FP8) {
+    L.qh = o;
+    o = up256(o + static_cast<size_t>(Tq) * kH * kD * 2);
+    L.wq = o;
+    o = up256(o + static_cast<size_t>(Tq) * kH * 4);
+  }
+  L.total = o;
+  return L;
+}
+
+// ------------------------------------------------------------------ ordering keys
+// 64-bit key: ordered fp32 score in the high word, ~position in the low word,
+// so that a larger key means (higher score, then lower position). Key 0 is
+// below every real key and marks an empty slot.
+__device__ __forceinline__ uint64_t make_key(float s, int pos) {
+  const uint32_t u = __float_as_uint(s + 0.0f);  // -0 -> +0
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(o) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(pos));
+}
+__device__ __forceinline__ float key_score(uint64_t key) {
+  const uint32_t o = static_cast<uint32_t>(key >> 32);
+  const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int key_pos(uint64_t key) {
+  return static_cast<int>(~static_cast<uint32_t>(key));
+}
+
+// ------------------------------------------------------------------ block scans (1024 threads)
+template <typename T>
+__device__ T block_excl_scan(T v, T* sm, T& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    T s = sm[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    sm[lane] = s;
+  }
+  __syncthreads();
+  const T excl = x - v + (w > 0 ? sm[w - 1] : T(0));
+  total = sm[31];
+  __syncthreads();
+  return excl;
+}
+
+// ------------------------------------------------------------------ plan
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
+                                                    const int32_t* __restrict__ cu_q, int B, int Tq,
+                                                    int QT, int NG, int causal, int max_pages, int k,
+                                                    char* ws, WsLayout L, int32_t* out_idx,
+                                                    float* out_score, unsigned int* status) {
+  __shared__ int smi[32];
+  __shared__ long long sml[32];
+  PlanHdr* hdr = reinterpret_cast<PlanHdr*>(ws + L.hdr);
+  int* qoff = reinterpret_cast<int*>(ws + L.seq_qoff);
+  int4* meta = reinterpret_cast<int4*>(ws + L.meta);
+  long long* prefix = reinterpret_cast<long long*>(ws + L.prefix);
+  int* cnt = reinterpret_cast<int*>(ws + L.counters);
+
+  int carry = 0;
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + threadIdx.x;
+    int v = 0;
+    if (b < B) {
+      const int q0 = cu_q[b], q1 = cu_q[b + 1], Ls = seq_lens[b];
+      const int nq = q1 - q0;
+      const bool ok = q0 >= 0 && nq >= 0 && q1 <= Tq && Ls >= nq &&
+                      static_cast<long long>(Ls) <= static_cast<long long>(max_pages) * 64;
+      if (!ok) atomicOr(status, DSA_DEV_BOUNDS);
+      v = ok ? (nq + QT - 1) / QT : 0;
+    }
+    int tot;
+    const int ex = block_excl_scan<int>(v, smi, tot);
+    if (b < B) qoff[b] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) qoff[B] = carry;
+  __syncthreads();
+  const int qtot = carry;
+
+  long long lcarry = 0;
+  for (int base = 0; base < qtot; base += 1024) {
+    const int qt = base + threadIdx.x;
+    long long cost = 0;
+    int4 m = make_int4(0, 0, 0, 0);
+    if (qt < qtot) {
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (qoff[mid] <= qt) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo;
+      const int t = qt - qoff[b];
+      const int q0 = cu_q[b], nq = cu_q[b + 1] - q0, Ls = seq_lens[b];
+      const int row0 = q0 + t * QT;
+      const int nrows = min(QT, nq - t * QT);
+      const int kend = causal ? (Ls - nq + t * QT + nrows) : Ls;
+      const int ntile = kend > 0 ? (kend + kTile - 1) / kTile : 0;
+      m = make_int4(b, row0, nrows, ntile);
+      meta[qt] = m;
+      cost = ntile;
+    }
+    long long tot;
+    const long long ex = block_excl_scan<long long>(cost, sml, tot);
+    if (qt < qtot) {
+      prefix[qt] = lcarry + ex;
+      for (int g = 0; g < NG; ++g) cnt[qt * NG + g] = 0;
+      if (m.w == 0) {  // no visible keys: the rows are all padding
+        for (int r = 0; r < m.z; ++r)
+          for (int i = 0; i < k; ++i) {
+            out_idx[static_cast<long long>(m.y + r) * k + i] = -1;
+            out_score[static_cast<long long>(m.y + r) * k + i] = -__int_as_float(0x7f800000);
+          }
+      }
+    }
+    lcarry += tot;
+  }
+  if (threadIdx.x == 0) {
+    prefix[qtot] = lcarry;
+    hdr->qtot = qtot;
+    hdr->total = lcarry;
+  }
+}
+
+// ------------------------------------------------------------------ fp8: queries -> f16
+// One warp per (query, head) row of 128 values. The power-of-two scale
+// 2^e puts the row's largest magnitude in [2^14, 2^15), so every bf16 value
+// within 2^31 of it converts to f16 exactly; w' = w * 2^-e undoes it after
+// the ReLU (relu(2^e x) = 2^e relu(x)).
+__global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
+                                                    const float* __restrict__ w,
+                                                    uint2* __restrict__ qh, float* __restrict__ wq,
+                                                    long long rows) {
+  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint2 v = q[r * 32 + lane];
+  float x[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)};
+  float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int e = 0;
+  if (m > 0.f) {
+    int ex;
+    frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
+    e = 15 - ex;
+  }
+  __half h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __float2half_rn(ldexpf(x[i], e));
+  uint2 o;
+  o.x = static_cast<uint32_t>(__half_as_ushort(h[0])) | (static_cast<uint32_t>(__half_as_ushort(h[1])) << 16);
+  o.y = static_cast<uint32_t>(__half_as_ushort(h[2])) | (static_cast<uint32_t>(__half_as_ushort(h[3])) << 16);
+  qh[r * 32 + lane] = o;
+  if (lane == 0) wq[r] = ldexpf(w[r], -e);
+}
+
+// ------------------------------------------------------------------ scorer configuration
+template <int QT, int FMT, int KSEL>
+struct Cfg {
+  static constexpr int N = 64 * QT;                      // MMA N: queries x heads
+  static constexpr int NG = QT == 4 ? 2 : 1;             // epilogue groups of 4 warps
+  static constexpr int QPG = QT / NG;                    // queries per group
+  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 2) : (FMT == DSA_FMT_BF16 ? 5 : 2);
+  static constexpr int SS = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // e4m3 staging
+  static constexpr int CAP = QT == 4 ? KSEL + 512 : 4 * KSEL;  // running top-k capacity
+  static constexpr int NEPI = 4 * NG;
+  static constexpr int NCONV = FMT == DSA_FMT_FP8 ? 4 : 0;
+  static constexpr int NWARPS = 2 + NEPI + NCONV;
+  static constexpr int NTHREADS = 32 * NWARPS;
+  static constexpr int TMEM_COLS = 2 * N;
+  static constexpr int Q_BYTES = N * 256;
+  static constexpr int OP_BYTES = kTile * 256;
+  static constexpr int STG_BYTES = kTile * 128;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_OP = OFF_Q + Q_BYTES;
+  static constexpr int OFF_STG = OFF_OP + S * OP_BYTES;
+  static constexpr int OFF_TOPK = OFF_STG + SS * STG_BYTES;
+  static constexpr int OFF_W = OFF_TOPK + QT * CAP * 8;
+  static constexpr int OFF_HIST = OFF_W + QT * 64 * 4;
+  static constexpr int OFF_MISC = OFF_HIST + NG * 256 * 4;
+  static constexpr int MISC_BYTES = 1024;
+  static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(CAP % 128 == 0, "capacity");
+};
+
+struct Misc {
+  uint64_t op_full[8], op_empty[8], stg_full[8], stg_empty[8];
+  uint64_t tm_full[2], tm_empty[2], q_full, q_empty, fin;
+  uint32_t tmem_base;
+  int abort;
+  int cnt[4];
+  unsigned long long thr[4];
+  int gok[2], glast[2], gdigit[2], gabove[2], gcd[2];
+  int wsum[2][2][4];
+};
+static_assert(sizeof(Misc) <= 1024, "misc");
+
+struct ScoreArgs {
+  const int32_t* page_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  int causal;
+  const uint8_t* cache;
+  int num_pages;
+  const float* w;  // head weights (fp8: with the query scale folded in)
+  const char* ws;
+  WsLayout L;
+  int32_t* out_idx;
+  float* out_score;
+  unsigned int* status;
+};
+
+struct Seg {
+  int qt, b, row0, nrows, ntile, t0, t1;
+  bool whole;
+};
+
+// Contiguous, equal share of the flattened (query tile, key tile) work.
+struct SegIter {
+  long long g, gbeg, gend;
+  int qt;
+  const long long* prefix;
+  const int4* meta;
+  __device__ void init(const long long* p, const int4* m, int qtot, long long total, int c, int G) {
+    prefix = p;
+    meta = m;
+    if (qtot <= 0 || total <= 0 || c >= G) {
+      g = gbeg = gend = 0;
+      qt = 0;
+      return;
+    }
+    gbeg = static_cast<long long>(c) * total / G;
+    gend = static_cast<long long>(c + 1) * total / G;
+    g = gbeg;
+    int lo = 0, hi = qtot - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    qt = lo;
+  }
+  __device__ bool next(Seg& s) {
+    if (g >= gend) return false;
+    while (prefix[qt + 1] <= g) ++qt;
+    const int4 m = meta[qt];
+    const long long p = prefix[qt];
+    s.qt = qt;
+    s.b = m.x;
+    s.row0 = m.y;
+    s.nrows = m.z;
+    s.ntile = m.w;
+    s.t0 = static_cast<int>(g - p);
+    const long long e = min(static_cast<long long>(m.w), gend - p);
+    s.t1 = static_cast<int>(e);
+    s.whole = (s.t0 == 0 && s.t1 == m.w);
+    g = p + e;
+    return true;
+  }
+};
+
+__device__ __forceinline__ long long range_start(int c, long long total, int G) {
+  return static_cast<long long>(c) * total / G;
+}
+__device__ __forceinline__ int owner_of(long long gtile, long long total, int G) {
+  int c = static_cast<int>(gtile * G / total);
+  while (c + 1 < G && range_start(c + 1, total, G) <= gtile) ++c;
+  while (c > 0 && range_start(c, total, G) > gtile) --c;
+  return c;
+}
+// A CTA keeps at most two partial lists: slot 2c for the query tile its
+// range starts in, 2c+1 for the one it ends in.
+__device__ __forceinline__ int partial_slot(int c, long long qt_start, long long total, int G) {
+  return range_start(c, total, G) >= qt_start ? 2 * c : 2 * c + 1;
+}
+
+// ------------------------------------------------------------------ running top-k (one group of 128 threads)
+__device__ __forceinline__ void push_key(bool pass, uint64_t key, uint64_t* buf, int* cnt, int lane) {
+  const unsigned m = __ballot_sync(0xffffffffu, pass);
+  if (m) {
+    const int leader = __ffs(m) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(cnt, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (pass) buf[base + __popc(m & ((1u << lane) - 1u))] = key;
+  }
+}
+
+// Keep exactly the K largest keys of buf[0..cnt) (when cnt > K): radix select
+// of the K-th largest key one byte at a time (histogram of the next byte of
+// the keys that match the prefix so far), then a stable in-place compaction.
+// The filter threshold becomes the selected prefix minus one.
+__device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, int K,
+                              uint32_t* hist, Misc* ms, int g, int gt, int barid) {
+  const int n = *cnt;
+  if (n <= K) return;
+  uint64_t prefix = 0, mask = 0;
+  int remaining = K;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = gt; i < 256; i += 128) hist[i] = 0;
+    named_bar(barid, 128);
+    for (int i = gt; i < n; i += 128) {
+      const uint64_t key = buf[i];
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    named_bar(barid, 128);
+    if (gt < 32) {
+      int c[8];
+      int sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        c[e] = static_cast<int>(hist[255 - 8 * gt - e]);
+        sum += c[e];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (gt >= o) incl += y;
+      }
+      const int excl = incl - sum;
+      if (excl < remaining && remaining <= incl) {
+        int acc = excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (acc + c[e] >= remaining) {
+            ms->gdigit[g] = 255 - 8 * gt - e;
+            ms->gabove[g] = acc;
+            ms->gcd[g] = c[e];
+            break;
+          }
+          acc += c[e];
+        }
+      }
+    }
+    named_bar(barid, 128);
+    const int d = ms->gdigit[g];
+    remaining -= ms->gabove[g];
+    const int cd = ms->gcd[g];
+    prefix |= static_cast<uint64_t>(d) << shift;
+    mask |= 255ull << shift;
+    if (cd == remaining) break;
+  }
+  const int w = gt >> 5, lane = gt & 31;
+  int base = 0;
+  for (int r0 = 0; r0 < n; r0 += 128) {
+    const int i = r0 + gt;
+    const uint64_t key = i < n ? buf[i] : 0ull;
+    const bool keep = i < n && key >= prefix;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    const int par = (r0 >> 7) & 1;
+    if (lane == 0) ms->wsum[g][par][w] = __popc(m);
+    named_bar(barid, 128);
+    int off = base, tot = 0;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int v = ms->wsum[g][par][x];
+      if (x < w) off += v;
+      tot += v;
+    }
+    if (keep) buf[off + __popc(m & ((1u << lane) - 1u))] = key;
+    base += tot;
+  }
+  named_bar(barid, 128);
+  if (gt == 0) {
+    *cnt = base;
+    *thr = prefix > 0 ? prefix - 1 : 0;
+  }
+  named_bar(barid, 128);
+}
+
+// ------------------------------------------------------------------ the scorer
+template <int QT, int FMT, int KSEL>
+__global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
+    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const ScoreArgs a) {
+  using C = Cfg<QT, FMT, KSEL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = sm + C::OFF_Q;
+  uint8_t* sOp = sm + C::OFF_OP;
+  uint8_t* sStg = sm + C::OFF_STG;
+  uint64_t* sTopk = reinterpret_cast<uint64_t*>(sm + C::OFF_TOPK);
+  float* sW = reinterpret_cast<float*>(sm + C::OFF_W);
+  uint32_t* sHist = reinterpret_cast<uint32_t*>(sm + C::OFF_HIST);
+  Misc* ms = reinterpret_cast<Misc*>(sm + C::OFF_MISC);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::S; ++i) {
+      mbar_init(&ms->op_full[i], FMT == DSA_FMT_BF16 ? 1 : 4);
+      mbar_init(&ms->op_empty[i], 1);
+    }
+    for (int i = 0; i < C::SS; ++i) {
+      mbar_init(&ms->stg_full[i], 1);
+      mbar_init(&ms->stg_empty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->tm_full[i], 1);
+      mbar_init(&ms->tm_empty[i], C::NEPI);
+    }
+    mbar_init(&ms->q_full, 1);
+    mbar_init(&ms->q_empty, 1);
+    mbar_init(&ms->fin, 1);
+    ms->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ms->tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = ms->tmem_base;
+
+  const PlanHdr* hdr = reinterpret_cast<const PlanHdr*>(a.ws + a.L.hdr);
+  const int4* meta = reinterpret_cast<const int4*>(a.ws + a.L.meta);
+  const long long* prefix = reinterpret_cast<const long long*>(a.ws + a.L.prefix);
+  const int qtot = hdr->qtot;
+  const long long total = hdr->total;
+  // CTAs c < Ge get non-empty, contiguous ranges of the flattened work;
+  // with Ge <= total every such range holds at least one tile.
+  const int Ge = total < G ? static_cast<int>(total) : G;
+  SegIter it;
+  it.init(prefix, meta, qtot, total, cta, Ge);
+  volatile int* abort_flag = &ms->abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    int tile_seq = 0, seg_i = 0;
+    Seg s;
+    bool stop = false;
+    while (!stop && it.next(s)) {
+      const int Ls = a.seq_lens[s.b];
+      const int npg = (Ls + 63) >> 6;
+      const int32_t* pt = a.page_table + static_cast<long long>(s.b) * a.max_pages;
+      if (lane == 0) {
+        if (!mbar_wait(&ms->q_empty, (seg_i & 1) ^ 1)) {
+          atomicOr(a.status, DSA_DEV_TIMEOUT);
+          *abort_flag = 1;
+        } else {
+          mbar_arrive_expect_tx(&ms->q_full, C::Q_BYTES);
+          tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
+          tma_load_2d(sQ + C::N * 128, &tm_q, 64, s.row0 * kH, &ms->q_full);
+        }
+      }
+      int pid0 = -1, pid1 = -1;
+      for (int t = s.t0; t < s.t1; ++t) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+          stop = true;
+          break;
+        }
+        const int rel = (t - s.t0) & 31;
+        if (rel == 0) {
+          const int tt = t + lane;
+          pid0 = -1;
+          pid1 = -1;
+          if (tt < s.t1) {
+            if (2 * tt < npg) pid0 = pt[2 * tt];
+            if (2 * tt + 1 < npg) pid1 = pt[2 * tt + 1];
+          }
+        }
+        const int p0 = __shfl_sync(0xffffffffu, pid0, rel);
+        const int p1 = __shfl_sync(0xffffffffu, pid1, rel);
+        if (lane == 0) {
+          const bool v0 = p0 >= 0 && p0 < a.num_pages;
+          const bool v1 = p1 >= 0 && p1 < a.num_pages;
+          if ((2 * t < npg && !v0) || (2 * t + 1 < npg && !v1)) atomicOr(a.status, DSA_DEV_BOUNDS);
+          if constexpr (FMT == DSA_FMT_BF16) {
+            const int slot = tile_seq % C::S, u = tile_seq / C::S;
+            if (!mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1)) {
+              atomicOr(a.status, DSA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            } else {
+              mbar_arrive_expect_tx(&ms->op_full[slot], (v0 + v1) * 16384);
+              uint8_t* dst = sOp + slot * C::OP_BYTES;
+              if (v0) {
+                tma_load_2d(dst, &tm_k, 0, p0 * 64, &ms->op_full[slot]);
+                tma_load_2d(dst + 16384, &tm_k, 64, p0 * 64, &ms->op_full[slot]);
+              }
+              if (v1) {
+                tma_load_2d(dst + 8192, &tm_k, 0, p1 * 64, &ms->op_full[slot]);
+                tma_load_2d(dst + 16384 + 8192, &tm_k, 64, p1 * 64, &ms->op_full[slot]);
+              }
+            }
+          } else {
+            const int slot = tile_seq % C::SS, u = tile_seq / C::SS;
+            if (!mbar_wait(&ms->stg_empty[slot], (u & 1) ^ 1)) {
+              atomicOr(a.status, DSA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            } else {
+              mbar_arrive_expect_tx(&ms->stg_full[slot], (v0 + v1) * 8192);
+              uint8_t* dst = sStg + slot * C::STG_BYTES;
+              if (v0) tma_load_3d(dst, &tm_k, 0, 0, p0, &ms->stg_full[slot]);
+              if (v1) tma_load_3d(dst + 8192, &tm_k, 0, 0, p1, &ms->stg_full[slot]);
+            }
+          }
+        }
+        ++tile_seq;
+      }
+      ++seg_i;
+    }
+    // on abort, let this CTA's copies in flight land before the CTA exits
+    if (lane == 0 && *abort_flag) {
+      constexpr int R = FMT == DSA_FMT_BF16 ? C::S : C::SS;
+      for (int i = 1; i <= R && tile_seq - i >= 0; ++i) {
+        const int ts = tile_seq - i;
+        uint64_t* fb = FMT == DSA_FMT_BF16 ? &ms->op_full[ts % R] : &ms->stg_full[ts % R];
+        mbar_wait(fb, (ts / R) & 1, 20000000LL);
+      }
+      mbar_wait(&ms->q_full, (seg_i - 1) & 1, 20000000LL);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, C::N, FMT == DSA_FMT_BF16);
+      int tile_seq = 0, seg_i = 0;
+      Seg s;
+      bool stop = false;
+      while (!stop && it.next(s)) {
+        if (!mbar_wait(&ms->q_full, seg_i & 1)) {
+          atomicOr(a.status, DSA_DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        for (int t = s.t0; t < s.t1; ++t) {
+          const int slot = tile_seq % C::S, u = tile_seq / C::S;
+          const int buf = tile_seq & 1, ub = tile_seq >> 1;
+          if (*abort_flag || !mbar_wait(&ms->op_full[slot], u & 1) ||
+              !mbar_wait(&ms->tm_empty[buf], (ub & 1) ^ 1)) {
+            if (!*abort_flag) atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sOp + slot * C::OP_BYTES);
+          const uint32_t b0 = smem_u32(sQ);
+          const uint32_t d = tbase + static_cast<uint32_t>(buf * C::N);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32);
+            const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
+            tc_mma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&ms->op_empty[slot]);
+          tc_commit(&ms->tm_full[buf]);
+          ++tile_seq;
+        }
+        tc_commit(&ms->q_empty);
+        ++seg_i;
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      tc_commit(&ms->fin);
+      mbar_wait(&ms->fin, 0, 200000000LL);
+    }
+  } else if (warp < 2 + C::NEPI) {
+    // ---------------------------------------------------------- epilogue
+    const int g = (warp - 2) >> 2;
+    const int gt = threadIdx.x - 32 * (2 + 4 * g);
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const int barid = 1 + g;
+    uint32_t* hist = sHist + g * 256;
+    int tile_seq = 0;
+    Seg s;
+    bool stop = false;
+    const long long qt_stride = C::NG;
+    int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
+    unsigned long long* partials =
+        reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
+    while (!stop && it.next(s)) {
+      const int Ls = a.seq_lens[s.b];
+      const int cq = a.cu_q[s.b];
+      const int nq = a.cu_q[s.b + 1] - cq;
+      const int32_t* pt = a.page_table + static_cast<long long>(s.b) * a.max_pages;
+      int lim[C::QPG];
+      unsigned long long thr[C::QPG];
+#pragma unroll
+      for (int jj = 0; jj < C::QPG; ++jj) {
+        const int j = g * C::QPG + jj;
+        if (gt == 0) {
+          ms->cnt[j] = 0;
+          ms->thr[j] = 0;
+        }
+        if (gt < 64) sW[j * 64 + gt] = j < s.nrows ? a.w[static_cast<long long>(s.row0 + j) * kH + gt] : 0.f;
+        lim[jj] = j < s.nrows ? (a.causal ? (Ls - nq + (s.row0 - cq) + j + 1) : Ls) : 0;
+        thr[jj] = 0;
+      }
+      named_bar(barid, 128);
+      for (int t = s.t0; t < s.t1; ++t) {
+        const int pos = t * kTile + row;
+        int pid = -1;
+        if (pos < Ls) {
+          pid = pt[pos >> 6];
+          if (pid < 0 || pid >= a.num_pages) pid = -1;
+        }
+        float kscale = 1.f;
+        if constexpr (FMT == DSA_FMT_FP8) {
+          if (pid >= 0)
+            kscale = __ldg(reinterpret_cast<const float*>(
+                a.cache + static_cast<long long>(pid) * kPageBytesFp8 + 64 * 128 + (pos & 63) * 4));
+        }
+        const int buf = tile_seq & 1, ub = tile_seq >> 1;
+        if (gt == 0) ms->gok[g] = mbar_wait(&ms->tm_full[buf], ub & 1) && !*abort_flag;
+        named_bar(barid, 128);
+        if (!ms->gok[g]) {
+          if (gt == 0) {
+            atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int jj = 0; jj < C::QPG; ++jj) {
+          const int j = g * C::QPG + jj;
+          const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) +
+                                 static_cast<uint32_t>(buf * C::N + j * 64);
+          const float4* w4 = reinterpret_cast<const float4*>(sW + j * 64);
+          float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+          float v[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            tmem_ld32(taddr + half * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 ww = w4[half * 8 + h4];
+              acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
+              acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
+              acc2 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc2);
+              acc3 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc3);
+            }
+          }
+          float sc = (acc0 + acc1) + (acc2 + acc3);
+          if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
+          const uint64_t key = make_key(sc, pos);
+          const bool pass = pid >= 0 && pos < lim[jj] && key > thr[jj];
+          push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->tm_empty[buf]);
+        named_bar(barid, 128);
+#pragma unroll
+        for (int jj = 0; jj < C::QPG; ++jj) {
+          const int j = g * C::QPG + jj;
+          if (ms->cnt[j] > C::CAP - kTile)
+            group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+          thr[jj] = ms->thr[j];
+        }
+        ++tile_seq;
+      }
+      if (stop) break;
+
+      // ------------------------------------------------ finish the segment
+      if (s.whole) {
+#pragma unroll
+        for (int jj = 0; jj < C::QPG; ++jj) {
+          const int j = g * C::QPG + jj;
+          group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+          if (j < s.nrows) {
+            const int n = min(ms->cnt[j], KSEL);
+            const long long o = static_cast<long long>(s.row0 + j) * KSEL;
+            for (int i = gt; i < KSEL; i += 128) {
+              if (i < n) {
+                const uint64_t key = sTopk[j * C::CAP + i];
+                a.out_idx[o + i] = key_pos(key);
+                a.out_score[o + i] = key_score(key);
+              } else {
+                a.out_idx[o + i] = -1;
+                a.out_score[o + i] = -__int_as_float(0x7f800000);
+              }
+            }
+          }
+        }
+      } else {
+        const long long qstart = prefix[s.qt];
+        const int slot = partial_slot(cta, qstart, total, Ge);
+#pragma unroll
+        for (int jj = 0; jj < C::QPG; ++jj) {
+          const int j = g * C::QPG + jj;
+          group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+          const int n = min(ms->cnt[j], KSEL);
+          unsigned long long* dst = partials + (static_cast<long long>(slot) * QT + j) * KSEL;
+          for (int i = gt; i < KSEL; i += 128) dst[i] = i < n ? sTopk[j * C::CAP + i] : 0ull;
+        }
+        __threadfence();
+        named_bar(barid, 128);
+        const int cf = owner_of(qstart, total, Ge);
+        const int cl = owner_of(prefix[s.qt + 1] - 1, total, Ge);
+        if (gt == 0) {
+          const int old = atomicAdd(&counters[s.qt * qt_stride + g], 1);
+          ms->glast[g] = (old == cl - cf);
+          __threadfence();
+        }
+        named_bar(barid, 128);
+        if (ms->glast[g]) {
+          // last piece of this query tile: merge every CTA's partial list
+#pragma unroll
+          for (int jj = 0; jj < C::QPG; ++jj) {
+            const int j = g * C::QPG + jj;
+            if (gt == 0) {
+              ms->cnt[j] = 0;
+              ms->thr[j] = 0;
+            }
+            named_bar(barid, 128);
+            unsigned long long th = 0;
+            for (int c = cf; c <= cl; ++c) {
+              const int sl = partial_slot(c, qstart, total, Ge);
+              const unsigned long long* src = partials + (static_cast<long long>(sl) * QT + j) * KSEL;
+              for (int r0 = 0; r0 < KSEL; r0 += 128) {
+                const unsigned long long key = __ldcg(src + r0 + gt);
+                push_key(key > th, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
+                named_bar(barid, 128);
+                if (ms->cnt[j] > C::CAP - kTile)
+                  group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+                th = ms->thr[j];
+                named_bar(barid, 128);  // every thread has read cnt before the next pushes
+              }
+            }
+            group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+            if (j < s.nrows) {
+              const int n = min(ms->cnt[j], KSEL);
+              const long long o = static_cast<long long>(s.row0 + j) * KSEL;
+              for (int i = gt; i < KSEL; i += 128) {
+                if (i < n) {
+                  const uint64_t key = sTopk[j * C::CAP + i];
+                  a.out_idx[o + i] = key_pos(key);
+                  a.out_score[o + i] = key_score(key);
+                } else {
+                  a.out_idx[o + i] = -1;
+                  a.out_score[o + i] = -__int_as_float(0x7f800000);
+                }
+              }
+            }
+          }
+        }
+      }
+      named_bar(barid, 128);
+    }
+  } else {
+    // ---------------------------------------------------------- fp8: e4m3 -> f16 converters
+    if constexpr (FMT == DSA_FMT_FP8) {
+      const int ct = threadIdx.x - 32 * (2 + C::NEPI);
+      int tile_seq = 0;
+      Seg s;
+      bool stop = false;
+      while (!stop && it.next(s)) {
+        for (int t = s.t0; t < s.t1; ++t) {
+          const int ss = tile_seq % C::SS, us = tile_seq / C::SS;
+          const int slot = tile_seq % C::S, u = tile_seq / C::S;
+          const bool ok = !*abort_flag && mbar_wait(&ms->stg_full[ss], us & 1) &&
+                          mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1);
+          if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              atomicOr(a.status, DSA_DEV_TIMEOUT);
+            }
+            stop = true;
+            break;
+          }
+          const uint8_t* src = sStg + ss * C::STG_BYTES;
+          uint8_t* dst = sOp + slot * C::OP_BYTES;
+#pragma unroll 2
+          for (int itn = 0; itn < 8; ++itn) {
+            const int idx = itn * 128 + ct;
+            const int r = idx >> 3, cb = idx & 7;
+            const uint4 e = *reinterpret_cast<const uint4*>(src + r * 128 + cb * 16);
+            const uint32_t wv[4] = {e.x, e.y, e.z, e.w};
+            uint32_t hv[8];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                  static_cast<__nv_fp8x2_storage_t>(wv[p] & 0xFFFFu), __NV_E4M3);
+              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                  static_cast<__nv_fp8x2_storage_t>(wv[p] >> 16), __NV_E4M3);
+              hv[2 * p] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
+              hv[2 * p + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
+            }
+            const int h = cb >> 2;
+            const int c0 = (cb & 3) * 2;
+            uint8_t* rowp = dst + h * 16384 + r * 128;
+            *reinterpret_cast<uint4*>(rowp + (((c0) ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&ms->op_full[slot]);
+            mbar_arrive(&ms->stg_empty[ss]);
+          }
+          ++tile_seq;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ row sort
+template <int K>
+__global__ void __launch_bounds__(256) sort_rows_kernel(int32_t* __restrict__ out_idx,
+                                                        float* __restrict__ out_score, int rows) {
+  constexpr int E = K / 32;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  int32_t* oi = out_idx + static_cast<long long>(r) * K;
+  float* os = out_score + static_cast<long long>(r) * K;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int idx = oi[e * 32 + lane];
+    v[e] = idx >= 0 ? make_key(os[e * 32 + lane], idx) : 0ull;
+  }
+#pragma unroll
+  for (int kk = 2; kk <= K; kk <<= 1) {
+#pragma unroll
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+      if (jj >= 32) {
+        const int je = jj >> 5;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int e2 = e ^ je;
+          if (e2 > e) {
+            const bool desc = ((e * 32) & kk) == 0;
+            const uint64_t x = v[e], y = v[e2];
+            const bool sw = desc ? (x < y) : (x > y);
+            v[e] = sw ? y : x;
+            v[e2] = sw ? x : y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], jj);
+          const bool lower = (lane & jj) == 0;
+          const bool desc = ((e * 32 + lane) & kk) == 0;
+          const uint64_t mx = v[e] > o ? v[e] : o;
+          const uint64_t mn = v[e] > o ? o : v[e];
+          v[e] = (lower == desc) ? mx : mn;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint64_t key = v[e];
+    oi[e * 32 + lane] = key ? key_pos(key) : -1;
+    os[e * 32 + lane] = key ? key_score(key) : -__int_as_float(0x7f800000);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+template <int QT, int FMT, int KSEL>
+dsa_status run_score(const CUtensorMap& tq, const CUtensorMap& tk, const ScoreArgs& args, int G,
+                     cudaStream_t stream) {
+  using C = Cfg<QT, FMT, KSEL>;
+  auto kern = score_kernel<QT, FMT, KSEL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  kern<<<G, C::NTHREADS, C::SMEM, stream>>>(tq, tk, args);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+template <int QT, int FMT>
+dsa_status run_score_k(int k, const CUtensorMap& tq, const CUtensorMap& tk, const ScoreArgs& args,
+                       int G, cudaStream_t stream) {
+  return k == 512 ? run_score<QT, FMT, 512>(tq, tk, args, G, stream)
+                  : run_score<QT, FMT, 1024>(tq, tk, args, G, stream);
+}
+
+}  // namespace
+
+size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt) {
+  return ws_layout(ctx->num_sms, Tq, B, k, fmt).total;
+}
+
+dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
+                       int32_t num_pages, dsa_fmt fmt, const int32_t* page_table,
+                       int32_t max_pages, const int32_t* seq_lens, const int32_t* cu_q,
+                       int32_t B, int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
+                       float* out_score, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws_bytes;
+  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, k, fmt);
+  char* ws = static_cast<char*>(workspace);
+  plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, cu_q, B, Tq, L.QT, L.NG, causal, max_pages, k, ws, L,
+                                      out_idx, out_score, ctx->status);
+  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+
+  const void* qsrc = q;
+  const float* wsrc = head_w;
+  const long long rows = static_cast<long long>(Tq) * kH;
+  if (fmt == DSA_FMT_FP8) {
+    const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+    qprep_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint2*>(q), head_w,
+                                             reinterpret_cast<uint2*>(ws + L.qh),
+                                             reinterpret_cast<float*>(ws + L.wq), rows);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    qsrc = ws + L.qh;
+    wsrc = reinterpret_cast<const float*>(ws + L.wq);
+  }
+
+  EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(ctx->encode_tiled);
+  CUtensorMap tq, tk;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD * 2)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(64 * L.QT)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tq, fmt == DSA_FMT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+            2, const_cast<void*>(qsrc), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return DSA_ERR_CUDA;
+  }
+  if (fmt == DSA_FMT_BF16) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_pages) * 64};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD * 2)};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return DSA_ERR_CUDA;
+  } else {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), 64, static_cast<cuuint64_t>(num_pages)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPageBytesFp8)};
+    const cuuint32_t box[3] = {128, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return DSA_ERR_CUDA;
+  }
+
+  ScoreArgs args;
+  args.page_table = page_table;
+  args.max_pages = max_pages;
+  args.seq_lens = seq_lens;
+  args.cu_q = cu_q;
+  args.causal = causal;
+  args.cache = static_cast<const uint8_t*>(cache);
+  args.num_pages = num_pages;
+  args.w = wsrc;
+  args.ws = ws;
+  args.L = L;
+  args.out_idx = out_idx;
+  args.out_score = out_score;
+  args.status = ctx->status;
+  const int G = L.G;
+  dsa_status st;
+  if (L.QT == 4)
+    st = fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(k, tq, tk, args, G, stream)
+                             : run_score_k<4, DSA_FMT_FP8>(k, tq, tk, args, G, stream);
+  else
+    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(k, tq, tk, args, G, stream)
+                             : run_score_k<1, DSA_FMT_FP8>(k, tq, tk, args, G, stream);
+  if (st != DSA_OK) return st;
+
+  const unsigned sblocks = static_cast<unsigned>((Tq + 7) / 8);
+  if (k == 512)
+    sort_rows_kernel<512><<<sblocks, 256, 0, stream>>>(out_idx, out_score, Tq);
+  else
+    sort_rows_kernel<1024><<<sblocks, 256, 0, stream>>>(out_idx, out_score, Tq);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

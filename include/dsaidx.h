@@ -1,0 +1,157 @@
+/*
+ * libdsaidx -- the DeepSeek Sparse Attention (DSA) indexer hot path on one
+ * GB300 GPU: the index-key store and the score + top-k selection.
+ *
+ * Sources (web pages on the bf16 index-K fix in the DSA indexer):
+ *  [VAL] "The Moment of Validation: Diagnosing an OOM Crash in the bf16 Index-K
+ *        Fix for DeepSeek V4 Sparse Attention", section "Input Knowledge
+ *        Required to Understand This Message": fp8 index keys take 128 bytes of
+ *        data plus a 4-byte scale (132 B/token), bf16 keys 128 x 2 = 256
+ *        B/token; the fused store normalises, applies RoPE and stores in one
+ *        kernel call.
+ *  [DEC] "The Fused Kernel Decision: Precision Archaeology in the CUDA Sparse
+ *        Attention Indexer", section "The Message": the indexer buffer is
+ *        paged, page_size = 64, [npages, 64*128] bf16; each token maps to a
+ *        page and an offset and its 128 values are written there.
+ *  [CRA] "The Crash That Changed Direction", sections "The Experiment: Why
+ *        fp32?" and "Assumptions Made and Broken": scores come from a batched
+ *        matrix product of queries and index keys followed by a ReLU; fp8
+ *        keys are up-converted exactly before the product; the top-512 (or
+ *        1024) key positions are kept.
+ *  [WFK] "When the Fused Kernel Isn't Enough", section "The Message:
+ *        Validation and Discovery": materialising the logits over the whole
+ *        context ran out of memory at about 22K tokens. This library never
+ *        materialises the [q_len x ctx] logits: key tiles stream through a
+ *        running per-query top-k.
+ *
+ * Conventions for every call:
+ *  - Pointers marked (device) are CUDA device pointers owned by the caller;
+ *    pointers marked (host) are host memory. The library keeps no pointer
+ *    after a call returns.
+ *  - Work is enqueued on `stream` and is asynchronous; argument errors are
+ *    returned before anything is enqueued. A launch failure returns
+ *    DSA_ERR_CUDA. Errors found on the device (a page id out of range, a
+ *    bounded wait that ran out) do not trap: the kernel skips the access,
+ *    records the error in a status word of the context and carries on;
+ *    dsa_get_device_status() reads and clears it.
+ *  - Sizes are int32 element counts; the byte layouts are stated per call.
+ *  - Index heads H = 64 and head_dim D = 128 are fixed. Page size is 64.
+ */
+#ifndef DSAIDX_H
+#define DSAIDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer ... */
+  DSA_ERR_UNSUPPORTED = 2,   /* k not in {512, 1024}, unknown format, no sm_103 device */
+  DSA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  DSA_ERR_DEVICE_BOUNDS = 4, /* device saw a page id / position / sequence out of range */
+  DSA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+  DSA_ERR_WORKSPACE = 6      /* workspace too small */
+} dsa_status;
+
+typedef enum {
+  DSA_FMT_BF16 = 0, /* 128 bf16 per token = 256 B; page = [64][128] bf16 = 16384 B      [DEC] */
+  DSA_FMT_FP8 = 1   /* 128 e4m3 + 1 fp32 scale = 132 B per token; page = [64][128] e4m3
+                       followed by [64] fp32 scales = 8448 B                            [VAL] */
+} dsa_fmt;
+
+enum { DSA_HEADS = 64, DSA_HEAD_DIM = 128, DSA_PAGE_SIZE = 64 };
+
+typedef struct dsa_ctx dsa_ctx; /* opaque; one per device */
+
+/* Create a context on the current CUDA device.
+ *  rope_theta  RoPE base theta (> 0); frequency of pair i is theta^(-2i/128).
+ *  rms_eps     RMSNorm epsilon (>= 0).
+ *  max_pos     positions the store accepts are 0 .. max_pos-1 (> 0). The
+ *              context holds a cos/sin table of max_pos x 64 x 8 bytes built
+ *              on the host in double precision and rounded to fp32.
+ *  gamma_bf16  (host) 128 bf16 RMSNorm weights, or NULL for all ones.
+ * Allocates device memory (the table, gamma, a status word). Returns
+ * DSA_ERR_UNSUPPORTED if the device is not compute capability 10.3. */
+dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_t max_pos,
+                          const uint16_t* gamma_bf16);
+
+/* Free the context's device memory. Synchronises the device first. */
+dsa_status dsa_ctx_destroy(dsa_ctx* ctx);
+
+/* Bytes per cache page for a format (16384 or 8448); 0 for an unknown format. */
+size_t dsa_cache_page_bytes(dsa_fmt fmt);
+
+/* Index-key store ([VAL], [DEC]): for each token t,
+ *   y  = RMSNorm(k_raw[t]) * gamma            (fp32, eps = rms_eps)
+ *   y' = RoPE(y, rope_pos[t])                 (dims i and i+64 rotated together)
+ *   written to page page_table[seq_id[t]][rope_pos[t] / 64], slot rope_pos[t] % 64:
+ *   bf16: round-to-nearest-even of y'; fp8: scale = max(max|y'|, 1e-4) / 448,
+ *   e4m3 (round to nearest even, saturating) of y' * (1/scale), and the scale.
+ * The fp32 operations follow one fixed order, so the stored bytes are
+ * reproducible bit for bit (sum of squares: 16 sequential partials over 8
+ * consecutive dims, then a pairwise tree; every product and sum of the
+ * rotation rounded separately).
+ *  k_raw       (device) [T][128] bf16, 16-byte aligned rows.
+ *  rope_pos    (device) [T] int32: the token's position in its sequence; also
+ *              its cache position. Must be in [0, min(max_pos, 64*max_pages)).
+ *  seq_id      (device) [T] int32 in [0, B).
+ *  page_table  (device) [B][max_pages] int32 page ids in [0, num_pages).
+ *  cache       (device) num_pages * dsa_cache_page_bytes(fmt) bytes, 256-byte aligned.
+ * Tokens must not share a slot within one call. Out-of-range seq/pos/page on
+ * the device: the token is skipped and DSA_ERR_DEVICE_BOUNDS is recorded. */
+dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_pos,
+                           const int32_t* seq_id, const int32_t* page_table, int32_t T,
+                           int32_t B, int32_t max_pages, void* cache, int32_t num_pages,
+                           dsa_fmt fmt, dsa_stream_t stream);
+
+/* Upper bound of the workspace bytes dsa_index_topk needs for these sizes.
+ * It does not grow with the context length: it holds the schedule
+ * (O(Tq + B)), split-context partial lists (O(#SMs * k)) and, for fp8
+ * caches, the queries converted for the tensor cores (O(Tq)). */
+size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k,
+                                     dsa_fmt fmt);
+
+/* Score + top-k ([CRA]): for each query row r of sequence b (rows
+ * cu_q[b] .. cu_q[b+1]-1, position p = seq_lens[b] - n_q(b) + j for the j-th),
+ *   s[r, key] = sum_h head_w[r][h] * max(0, sum_d q[r][h][d] * k[key][d])
+ * over the visible keys of sequence b: positions 0..p when causal, else
+ * 0..seq_lens[b]-1; k is the stored key (fp8: e4m3 value times its scale).
+ * Output row r holds the positions (within the sequence) and fp32 scores of
+ * the min(k, visible) best keys, ordered by (score desc, position asc);
+ * unused slots are -1 / -inf.
+ *  q           (device) [Tq][64][128] bf16, 16-byte aligned.
+ *  head_w      (device) [Tq][64] fp32.
+ *  cache       (device) as written by dsa_index_store, num_pages pages of fmt.
+ *  page_table  (device) [B][max_pages] int32; entries past a sequence's last
+ *              page are not read.
+ *  seq_lens    (device) [B] int32, n_q(b) <= seq_lens[b] <= 64*max_pages.
+ *  cu_q        (device) [B+1] int32, cu_q[0] = 0, non-decreasing, cu_q[B] = Tq.
+ *  k           512 or 1024.
+ *  out_idx     (device) [Tq][k] int32;  out_score (device) [Tq][k] fp32.
+ *  workspace   (device) >= dsa_index_topk_workspace_size(...) bytes, 256-byte
+ *              aligned; contents need not be initialised and are scratch.
+ * Scratch memory is O(#SMs * tile) + O(Tq * k): the logits are never stored. */
+dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
+                          int32_t num_pages, dsa_fmt fmt, const int32_t* page_table,
+                          int32_t max_pages, const int32_t* seq_lens, const int32_t* cu_q,
+                          int32_t B, int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
+                          float* out_score, void* workspace, size_t ws_bytes,
+                          dsa_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the context's device status
+ * word. Returns DSA_OK or the first device-side error recorded. */
+dsa_status dsa_get_device_status(dsa_ctx* ctx, dsa_stream_t stream);
+
+/* Static string for a status code. */
+const char* dsa_status_str(dsa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSAIDX_H */

@@ -59,7 +59,8 @@ def rope_cos_sin(theta: float, positions: np.ndarray):
     """fp32 cos/sin of pos * theta^(-2i/128) for i < 64, from double libm."""
     positions = np.asarray(positions, dtype=np.int64)
     uniq, inv = np.unique(positions, return_inverse=True)
-    freqs = [math.pow(float(theta), -(2.0 * i) / D) for i in range(HALF)]
+    th = float(np.float32(theta))            # theta is an fp32 parameter of the store
+    freqs = [math.pow(th, -(2.0 * i) / D) for i in range(HALF)]
     cu = np.empty((len(uniq), HALF), dtype=np.float32)
     su = np.empty((len(uniq), HALF), dtype=np.float32)
     for r, p in enumerate(uniq.tolist()):

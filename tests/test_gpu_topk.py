@@ -1,0 +1,138 @@
+"""GPU parity of dsa_index_topk against the oracle.
+
+Rules (tests/parity.py): equal top-k sets except swaps within 1e-3 * max|s|
+of the oracle's k-th score; logits within 2e-3 (bf16) / 3e-2 (fp8) of the
+oracle relative to the row's largest top-k score; rows sorted by (score
+desc, position asc); -1 / -inf padding.
+"""
+import numpy as np
+import pytest
+
+from oracle import indexer as X
+from oracle import store as S
+from synth import inputs as I
+from tests import gpu_util as U
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [S.FMT_BF16, S.FMT_FP8]
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import torch
+    from dsa_sparse_attention_store_gb300 import Context
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    c = Context(theta=10000.0, eps=1e-6, max_pos=131072)
+    yield c
+    c.close()
+
+
+def _check(wl, fmt, ctx, rows=None, k=None):
+    k = wl.k if k is None else k
+    d = U.device_workload(wl, fmt, ctx)
+    gi, gs = U.run_topk(wl, fmt, ctx, d, k)
+    assert ctx.device_status() == 0
+    rows = np.arange(wl.Tq) if rows is None else np.asarray(rows)
+    cache = U.oracle_cache(wl, fmt)
+    oi, os_, full = U.oracle_topk(wl, fmt, cache, rows, k)
+    ok, reps = P.compare(rows, gi[rows], gs[rows], oi, os_, full, k, fmt)
+    assert ok, P.summary(reps)
+    return gi, gs, reps
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_prefill_multi_sequence_ragged(ctx, fmt):
+    # three causal prefills whose lengths end mid-tile and mid-page
+    wl = I.make_workload("pf", [300, 777, 129], [300, 777, 129], [300, 777, 129], True, 512,
+                         seed=31, wid=30)
+    _check(wl, fmt, ctx)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_decode_batch_split_contexts(ctx, fmt):
+    # one query per sequence (the decode path), contexts split across CTAs
+    rng = np.random.default_rng(3)
+    L = rng.integers(100, 6000, 24)
+    wl = I.make_workload("dc", L, [1] * 24, [1] * 24, True, 512, seed=32, wid=31)
+    _check(wl, fmt, ctx)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_long_context_k1024_many_pieces(ctx, fmt):
+    # 8 queries per sequence, k=1024, each query tile spread over many CTAs
+    wl = I.make_workload("ld", [20000, 9000], [8, 8], [64, 64], True, 1024, seed=33, wid=32)
+    _check(wl, fmt, ctx)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_non_causal(ctx, fmt):
+    wl = I.make_workload("nc", [1000, 450], [13, 7], [1000, 450], False, 512, seed=34, wid=33)
+    _check(wl, fmt, ctx)
+
+
+def test_short_contexts_take_all_keys(ctx):
+    wl = I.make_workload("sh", [5, 300, 1000], [5, 3, 2], [5, 300, 1000], True, 1024, seed=35, wid=34)
+    gi, _, _ = _check(wl, 0, ctx)
+    for r in range(wl.Tq):
+        n = X.visible_count(wl.cu_q, wl.seq_lens, r, True)
+        if n <= 1024:
+            assert set(gi[r][gi[r] >= 0].tolist()) == set(range(n))
+
+
+def test_zero_queries_tie_break_by_position(ctx):
+    # all scores are exactly 0: the k lowest positions win, in order
+    wl = I.make_workload("z", [2000], [4], [2000], True, 512, seed=36, wid=35)
+    wl.q[:] = 0
+    gi, gs, _ = _check(wl, 0, ctx)
+    assert np.array_equal(gi, np.tile(np.arange(512, dtype=np.int32), (4, 1)))
+    assert np.all(gs == 0)
+
+
+def test_sequence_without_queries_and_mixed_counts(ctx):
+    wl = I.make_workload("mx", [700, 300, 2500], [0, 300, 1], [700, 300, 2500], True, 512,
+                         seed=37, wid=36)
+    _check(wl, 1, ctx)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_tiny_prefill_config(ctx, fmt):
+    # 1 sequence, 1024 tokens, all queries causal, k=512 (the smallest workload)
+    _check(I.tiny_prefill(), fmt, ctx)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_batched_decode_config(ctx, fmt):
+    # 64 sequences x 1 query, contexts U[2048, 16384], permuted pages, k=512
+    _check(I.batched_decode(), fmt, ctx)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_needle_config(ctx, fmt):
+    wl = I.needle()
+    rows = np.concatenate([np.array(wl.needle_queries), np.arange(0, wl.Tq - 64, 331)])
+    gi, _, _ = _check(wl, fmt, ctx, rows=rows)
+    for r in wl.needle_queries:
+        sel = set(gi[r].tolist())
+        for p in wl.needles:
+            assert p in sel, f"needle at {p} missing for query {r}"
+
+
+def test_long_prefill_config_sampled(ctx):
+    # the 22528-token causal prefill: sampled rows against the oracle, and
+    # the scratch stays O(#SMs * tile + Tq * k)
+    import torch
+    wl = I.long_prefill()
+    ws = ctx.topk_workspace_size(wl.Tq, wl.B, wl.k, 0)
+    assert ws < 64 << 20
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([[0, 1, 127, 128, 511, 512, 513, wl.Tq - 1],
+                                   rng.choice(wl.Tq, 40, replace=False)]))
+    _check(wl, 0, ctx, rows=rows)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_long_decode_config_sampled(ctx, fmt):
+    wl = I.long_decode()
+    _check(wl, fmt, ctx, rows=np.arange(wl.Tq))
