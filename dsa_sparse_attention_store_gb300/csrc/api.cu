@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "internal.cuh"
@@ -77,7 +78,7 @@ dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_
     }
   }
 
-  dsa_ctx* c = static_cast<dsa_ctx*>(std::calloc(1, sizeof(dsa_ctx)));
+  dsa_ctx* c = new (std::nothrow) dsa_ctx();
   if (!c) return DSA_ERR_CUDA;
   c->device = dev;
   c->num_sms = sms;
@@ -95,7 +96,7 @@ dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_
     cudaFree(c->rope);
     cudaFree(c->gamma);
     cudaFree(c->status);
-    std::free(c);
+    delete c;
     return DSA_ERR_CUDA;
   }
   *out = c;
@@ -108,7 +109,46 @@ dsa_status dsa_ctx_destroy(dsa_ctx* ctx) {
   cudaFree(ctx->rope);
   cudaFree(ctx->gamma);
   cudaFree(ctx->status);
-  std::free(ctx);
+  if (ctx->prof) {
+    for (int i = 0; i < dsa::kProfCap; ++i) {
+      cudaEventDestroy(ctx->prof[i].ev0);
+      cudaEventDestroy(ctx->prof[i].ev1);
+    }
+    delete[] ctx->prof;
+  }
+  delete ctx;
+  return DSA_OK;
+}
+
+dsa_status dsa_profile_enable(dsa_ctx* ctx, int on) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  if (on && !ctx->prof) {
+    ctx->prof = new (std::nothrow) dsa_prof_rec[dsa::kProfCap];
+    if (!ctx->prof) return DSA_ERR_CUDA;
+    for (int i = 0; i < dsa::kProfCap; ++i) {
+      if (cudaEventCreate(&ctx->prof[i].ev0) != cudaSuccess ||
+          cudaEventCreate(&ctx->prof[i].ev1) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    }
+  }
+  ctx->prof_on = on ? 1 : 0;
+  return DSA_OK;
+}
+
+dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms, int32_t* launches) {
+  if (!ctx || !ms || !launches) return DSA_ERR_INVALID_ARG;
+  for (int k = 0; k < DSA_K_COUNT; ++k) {
+    ms[k] = 0.f;
+    launches[k] = static_cast<int32_t>(ctx->launches[k]);
+    ctx->launches[k] = 0;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return DSA_ERR_CUDA;
+  for (int i = 0; i < ctx->prof_n; ++i) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, ctx->prof[i].ev0, ctx->prof[i].ev1) != cudaSuccess) return DSA_ERR_CUDA;
+    ms[ctx->prof[i].kind] += t;
+  }
+  ctx->prof_n = 0;
   return DSA_OK;
 }
 

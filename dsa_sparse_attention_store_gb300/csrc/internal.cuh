@@ -11,6 +11,11 @@
 #define DSA_DEV_BOUNDS 1u
 #define DSA_DEV_TIMEOUT 2u
 
+struct dsa_prof_rec {
+  int kind;
+  cudaEvent_t ev0, ev1;
+};
+
 struct dsa_ctx {
   int device;
   int num_sms;
@@ -21,7 +26,34 @@ struct dsa_ctx {
   float* gamma;          // [128]
   unsigned int* status;  // device status word
   void* encode_tiled;    // cuTensorMapEncodeTiled entry point
+  // kernel timing (dsa_profile_*)
+  int prof_on;
+  int prof_n;                    // records in use
+  dsa_prof_rec* prof;            // kProfCap records, events created on enable
+  long long launches[DSA_K_COUNT];
 };
+
+namespace dsa {
+constexpr int kProfCap = 8192;
+// Record the start/end of one kernel launch of kind `kind` on `stream`.
+struct LaunchScope {
+  dsa_ctx* ctx;
+  int kind;
+  dsa_prof_rec* rec;
+  cudaStream_t stream;
+  LaunchScope(dsa_ctx* c, int k, cudaStream_t s) : ctx(c), kind(k), rec(nullptr), stream(s) {
+    ctx->launches[kind] += 1;
+    if (ctx->prof_on && ctx->prof_n < kProfCap) {
+      rec = &ctx->prof[ctx->prof_n++];
+      rec->kind = kind;
+      cudaEventRecord(rec->ev0, stream);
+    }
+  }
+  ~LaunchScope() {
+    if (rec) cudaEventRecord(rec->ev1, stream);
+  }
+};
+}  // namespace dsa
 
 namespace dsa {
 

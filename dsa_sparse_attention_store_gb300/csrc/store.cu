@@ -145,6 +145,7 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
   if (T == 0) return DSA_OK;
   const long long threads = static_cast<long long>(T) * 16;
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  LaunchScope scope(ctx, DSA_K_STORE, stream);
   if (fmt == DSA_FMT_BF16)
     store_kernel<DSA_FMT_BF16><<<blocks, 256, 0, stream>>>(
         static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B, max_pages,

@@ -47,7 +47,6 @@ namespace {
 constexpr int kH = 64;
 constexpr int kD = 128;
 constexpr int kTile = 128;  // keys per MMA tile = 2 pages
-constexpr int kPageBytesBf16 = 64 * 128 * 2;
 constexpr int kPageBytesFp8 = 64 * 128 + 64 * 4;
 
 struct PlanHdr {
@@ -975,21 +974,22 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 template <int QT, int FMT, int KSEL>
-dsa_status run_score(const CUtensorMap& tq, const CUtensorMap& tk, const ScoreArgs& args, int G,
-                     cudaStream_t stream) {
+dsa_status run_score(dsa_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const ScoreArgs& args, int G, cudaStream_t stream) {
   using C = Cfg<QT, FMT, KSEL>;
   auto kern = score_kernel<QT, FMT, KSEL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return DSA_ERR_CUDA;
+  LaunchScope scope(ctx, FMT == DSA_FMT_BF16 ? DSA_K_SCORE_BF16 : DSA_K_SCORE_FP8, stream);
   kern<<<G, C::NTHREADS, C::SMEM, stream>>>(tq, tk, args);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 template <int QT, int FMT>
-dsa_status run_score_k(int k, const CUtensorMap& tq, const CUtensorMap& tk, const ScoreArgs& args,
-                       int G, cudaStream_t stream) {
-  return k == 512 ? run_score<QT, FMT, 512>(tq, tk, args, G, stream)
-                  : run_score<QT, FMT, 1024>(tq, tk, args, G, stream);
+dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const ScoreArgs& args, int G, cudaStream_t stream) {
+  return k == 512 ? run_score<QT, FMT, 512>(ctx, tq, tk, args, G, stream)
+                  : run_score<QT, FMT, 1024>(ctx, tq, tk, args, G, stream);
 }
 
 }  // namespace
@@ -1006,8 +1006,11 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   (void)ws_bytes;
   const WsLayout L = ws_layout(ctx->num_sms, Tq, B, k, fmt);
   char* ws = static_cast<char*>(workspace);
-  plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, cu_q, B, Tq, L.QT, L.NG, causal, max_pages, k, ws, L,
-                                      out_idx, out_score, ctx->status);
+  {
+    LaunchScope scope(ctx, DSA_K_PLAN, stream);
+    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, cu_q, B, Tq, L.QT, L.NG, causal, max_pages, k, ws,
+                                        L, out_idx, out_score, ctx->status);
+  }
   if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
 
   const void* qsrc = q;
@@ -1015,9 +1018,12 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   const long long rows = static_cast<long long>(Tq) * kH;
   if (fmt == DSA_FMT_FP8) {
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
-    qprep_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint2*>(q), head_w,
-                                             reinterpret_cast<uint2*>(ws + L.qh),
-                                             reinterpret_cast<float*>(ws + L.wq), rows);
+    {
+      LaunchScope scope(ctx, DSA_K_QPREP, stream);
+      qprep_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint2*>(q), head_w,
+                                               reinterpret_cast<uint2*>(ws + L.qh),
+                                               reinterpret_cast<float*>(ws + L.wq), rows);
+    }
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     qsrc = ws + L.qh;
     wsrc = reinterpret_cast<const float*>(ws + L.wq);
@@ -1073,14 +1079,15 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   const int G = L.G;
   dsa_status st;
   if (L.QT == 4)
-    st = fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(k, tq, tk, args, G, stream)
-                             : run_score_k<4, DSA_FMT_FP8>(k, tq, tk, args, G, stream);
+    st = fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
+                             : run_score_k<4, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
   else
-    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(k, tq, tk, args, G, stream)
-                             : run_score_k<1, DSA_FMT_FP8>(k, tq, tk, args, G, stream);
+    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
+                             : run_score_k<1, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
   if (st != DSA_OK) return st;
 
   const unsigned sblocks = static_cast<unsigned>((Tq + 7) / 8);
+  LaunchScope scope(ctx, DSA_K_SORT, stream);
   if (k == 512)
     sort_rows_kernel<512><<<sblocks, 256, 0, stream>>>(out_idx, out_score, Tq);
   else

@@ -13,6 +13,7 @@ import os
 
 FMT_BF16 = 0
 FMT_FP8 = 1
+KERNEL_KINDS = ("store", "plan", "qprep", "score_bf16", "score_fp8", "sort")
 HEADS = 64
 HEAD_DIM = 128
 PAGE_SIZE = 64
@@ -56,6 +57,10 @@ def lib() -> ctypes.CDLL:
         L.dsa_index_topk.restype = ctypes.c_int
         L.dsa_get_device_status.argtypes = [_c_ptr, _c_ptr]
         L.dsa_get_device_status.restype = ctypes.c_int
+        L.dsa_profile_enable.argtypes = [_c_ptr, ctypes.c_int]
+        L.dsa_profile_enable.restype = ctypes.c_int
+        L.dsa_profile_read.argtypes = [_c_ptr, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_c_int)]
+        L.dsa_profile_read.restype = ctypes.c_int
         L.dsa_status_str.argtypes = [ctypes.c_int]
         L.dsa_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -169,6 +174,20 @@ class Context:
             _stream_ptr(stream))
         if st != 0:
             raise DsaError("dsa_index_topk", st)
+
+    def profile_enable(self, on: bool = True):
+        st = lib().dsa_profile_enable(self._h, 1 if on else 0)
+        if st != 0:
+            raise DsaError("dsa_profile_enable", st)
+
+    def profile_read(self):
+        """{kind: (total ms, launches)} since the previous read (synchronises)."""
+        ms = (ctypes.c_float * len(KERNEL_KINDS))()
+        n = (_c_int * len(KERNEL_KINDS))()
+        st = lib().dsa_profile_read(self._h, ms, n)
+        if st != 0:
+            raise DsaError("dsa_profile_read", st)
+        return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(KERNEL_KINDS)}
 
     def device_status(self, stream=None) -> int:
         """Synchronise the stream; read and clear the device status word."""

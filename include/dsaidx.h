@@ -144,6 +144,25 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
                           float* out_score, void* workspace, size_t ws_bytes,
                           dsa_stream_t stream);
 
+/* Kernel timing, for benchmarks and profiling. While enabled, the library
+ * records a CUDA event pair on the launch stream around each kernel it
+ * launches (at most 8192 pairs between reads; later launches are counted but
+ * not timed). dsa_profile_read synchronises the device, writes per-kind total
+ * milliseconds and launch counts since the previous read (launches are
+ * counted whether or not timing is on), and resets both. */
+typedef enum {
+  DSA_K_STORE = 0,      /* dsa_index_store */
+  DSA_K_PLAN = 1,       /* dsa_index_topk: schedule */
+  DSA_K_QPREP = 2,      /* dsa_index_topk, fp8 only: query conversion */
+  DSA_K_SCORE_BF16 = 3, /* dsa_index_topk: tensor-core scorer + running top-k, bf16 cache */
+  DSA_K_SCORE_FP8 = 4,  /* the same, fp8 cache */
+  DSA_K_SORT = 5,       /* dsa_index_topk: per-row sort */
+  DSA_K_COUNT = 6
+} dsa_kernel_kind;
+dsa_status dsa_profile_enable(dsa_ctx* ctx, int on);
+dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms /* [DSA_K_COUNT] */,
+                            int32_t* launches /* [DSA_K_COUNT] */);
+
 /* Synchronise `stream`, then read and clear the context's device status
  * word. Returns DSA_OK or the first device-side error recorded. */
 dsa_status dsa_get_device_status(dsa_ctx* ctx, dsa_stream_t stream);

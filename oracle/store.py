@@ -132,6 +132,18 @@ def slots(pos: np.ndarray, seq: np.ndarray, page_table: np.ndarray, num_pages: i
     return page, pos % PAGE
 
 
+def _views(cache: np.ndarray, fmt: int):
+    """Per-page views of the cache bytes: bf16 -> [pages, 64, 256] bytes;
+    fp8 -> ([pages, 64, 128] codes, [pages, 64] fp32 scales)."""
+    pb = PAGE_BYTES[fmt]
+    pages = cache.reshape(-1, pb)
+    if fmt == FMT_BF16:
+        return pages.reshape(-1, PAGE, 2 * D), None
+    data = pages[:, :PAGE * D].reshape(-1, PAGE, D)
+    scales = pages[:, PAGE * D:].view("<f4")
+    return data, scales
+
+
 def store(cache: np.ndarray, fmt: int, k_raw_bits, pos, seq, page_table, num_pages: int,
           theta: float = 10000.0, eps: float = 1e-6, gamma_bits=None) -> None:
     """Write the tokens' index keys into the byte image of the paged cache."""
@@ -139,18 +151,13 @@ def store(cache: np.ndarray, fmt: int, k_raw_bits, pos, seq, page_table, num_pag
         return
     yr = normalize_rotate(k_raw_bits, pos, theta, eps, gamma_bits)
     page, off = slots(pos, seq, page_table, num_pages)
-    pb = PAGE_BYTES[fmt]
+    data, scales = _views(cache, fmt)
     if fmt == FMT_BF16:
-        b = F.f32_to_bf16(yr).view(np.uint8).reshape(-1, 2 * D)
-        base = page * pb + off * 2 * D
-        idx = base[:, None] + np.arange(2 * D)[None, :]
-        cache[idx] = b
+        data[page, off] = F.f32_to_bf16(yr).view(np.uint8).reshape(-1, 2 * D)
     else:
         codes, scale = quantize_fp8(yr)
-        base = page * pb + off * D
-        cache[base[:, None] + np.arange(D)[None, :]] = codes
-        sb = page * pb + PAGE * D + off * 4
-        cache[sb[:, None] + np.arange(4)[None, :]] = scale.astype("<f4").view(np.uint8).reshape(-1, 4)
+        data[page, off] = codes
+        scales[page, off] = scale
 
 
 def read_keys(cache: np.ndarray, fmt: int, page_table_row: np.ndarray, n: int) -> np.ndarray:
@@ -161,13 +168,7 @@ def read_keys(cache: np.ndarray, fmt: int, page_table_row: np.ndarray, n: int) -
     pos = np.arange(n, dtype=np.int64)
     page = np.asarray(page_table_row, dtype=np.int64)[pos // PAGE]
     off = pos % PAGE
-    pb = PAGE_BYTES[fmt]
+    data, scales = _views(cache, fmt)
     if fmt == FMT_BF16:
-        base = page * pb + off * 2 * D
-        raw = cache[base[:, None] + np.arange(2 * D)[None, :]]
-        return F.bf16_to_f64(raw.copy().view(np.uint16))
-    base = page * pb + off * D
-    codes = cache[base[:, None] + np.arange(D)[None, :]]
-    sb = page * pb + PAGE * D + off * 4
-    scale = cache[sb[:, None] + np.arange(4)[None, :]].copy().view("<f4").reshape(-1).astype(np.float64)
-    return F.e4m3_to_f64(codes) * scale[:, None]
+        return F.bf16_to_f64(np.ascontiguousarray(data[page, off]).view(np.uint16))
+    return F.e4m3_to_f64(data[page, off]) * scales[page, off].astype(np.float64)[:, None]
