@@ -55,6 +55,10 @@ def lib() -> ctypes.CDLL:
                                      _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
                                      _c_ptr, _c_size, _c_ptr]
         L.dsa_index_topk.restype = ctypes.c_int
+        L.dsa_index_topk_static.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, ctypes.c_int, _c_ptr,
+                                            _c_int, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
+                                            _c_ptr, _c_ptr, _c_ptr]
+        L.dsa_index_topk_static.restype = ctypes.c_int
         L.dsa_get_device_status.argtypes = [_c_ptr, _c_ptr]
         L.dsa_get_device_status.restype = ctypes.c_int
         L.dsa_profile_enable.argtypes = [_c_ptr, ctypes.c_int]
@@ -174,6 +178,24 @@ class Context:
             _stream_ptr(stream))
         if st != 0:
             raise DsaError("dsa_index_topk", st)
+
+    def topk_static(self, q, head_w, cache, num_pages: int, fmt: int, page_table, seq_lens, cu_q,
+                    causal: bool, k: int, out_idx, out_score, stream=None):
+        """dsa_index_topk_static: as topk(), with the library's fixed scratch
+        array instead of a caller workspace (allocates nothing)."""
+        import torch
+        Tq = int(q.shape[0])
+        B, max_pages = int(page_table.shape[0]), int(page_table.shape[1])
+        st = lib().dsa_index_topk_static(
+            self._h, _dev(q, torch.bfloat16, (Tq, HEADS, HEAD_DIM), "q"),
+            _dev(head_w, torch.float32, (Tq, HEADS), "head_w"), _dev(cache, torch.uint8, None, "cache"),
+            _c_int(num_pages), int(fmt), _dev(page_table, torch.int32, None, "page_table"),
+            _c_int(max_pages), _dev(seq_lens, torch.int32, (B,), "seq_lens"),
+            _dev(cu_q, torch.int32, (B + 1,), "cu_q"), _c_int(B), _c_int(Tq), _c_int(1 if causal else 0),
+            _c_int(k), _dev(out_idx, torch.int32, (Tq, k), "out_idx"),
+            _dev(out_score, torch.float32, (Tq, k), "out_score"), _stream_ptr(stream))
+        if st != 0:
+            raise DsaError("dsa_index_topk_static", st)
 
     def profile_enable(self, on: bool = True):
         st = lib().dsa_profile_enable(self._h, 1 if on else 0)

@@ -144,6 +144,31 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
                           float* out_score, void* workspace, size_t ws_bytes,
                           dsa_stream_t stream);
 
+/* Allocation-free top-k, for callers that cannot allocate device memory
+ * (an engine whose memory is already carved into its own pools, or a
+ * latency-critical path that must not call cudaMalloc). The paper has no
+ * counterpart; it is an addition of this library.
+ * Same arguments and results as dsa_index_topk, without the workspace: the
+ * scratch is a fixed array of DSA_STATIC_WORKSPACE_BYTES in the library's
+ * device image, held by every GPU that loads the library until exit. The
+ * call allocates nothing. Its first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture. All calls share the array: calls that overlap on the GPU
+ * race. Nothing in it needs clearing; each call rewrites what must start at
+ * zero. Returns DSA_ERR_WORKSPACE, without launching anything, when
+ * dsa_index_topk_workspace_size(ctx, Tq, B, k, fmt) exceeds
+ * DSA_STATIC_WORKSPACE_BYTES (on a 152-SM GB300 with one sequence: bf16
+ * batches up to about 2.9M queries; fp8 batches up to 1417 queries with
+ * k = 1024 and 1716 with k = 512, since fp8 caches keep the converted
+ * queries, 16.6 KB each, in the scratch). */
+#define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
+dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_w,
+                                 const void* cache, int32_t num_pages, dsa_fmt fmt,
+                                 const int32_t* page_table, int32_t max_pages,
+                                 const int32_t* seq_lens, const int32_t* cu_q, int32_t B,
+                                 int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
+                                 float* out_score, dsa_stream_t stream);
+
 /* Kernel timing, for benchmarks and profiling. While enabled, the library
  * records a CUDA event pair on the launch stream around each kernel it
  * launches (at most 8192 pairs between reads; later launches are counted but

@@ -1,0 +1,79 @@
+"""GPU test of dsa_index_topk_static, the top-k entry point for callers that
+cannot allocate device memory (an engine that has already split all free
+memory into its own pools, or a latency-critical path where cudaMalloc is not
+allowed). It must give the same results as dsa_index_topk with a caller
+workspace, on two calls in a row that share its fixed scratch array, and
+reject sizes beyond that array without launching.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from synth import inputs as I
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+def _call_static(ctx, wl, fmt, d, k, out_i, out_s):
+    from dsa_sparse_attention_store_gb300 import dsaidx
+    import torch
+    L = dsaidx.lib()
+    P = ctypes.c_void_p
+    st = L.dsa_index_topk_static(
+        ctx.handle, P(d["q"].data_ptr()), P(d["head_w"].data_ptr()), P(d["cache"].data_ptr()),
+        wl.num_pages, fmt, P(d["page_table"].data_ptr()), wl.max_pages, P(d["seq_lens"].data_ptr()),
+        P(d["cu_q"].data_ptr()), wl.B, wl.Tq, 1 if wl.causal else 0, k, P(out_i.data_ptr()),
+        P(out_s.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
+    return st
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_static_scratch_matches_workspace_path(fmt):
+    import torch
+    from dsa_sparse_attention_store_gb300 import Context
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    ctx = Context(theta=10000.0, eps=1e-6, max_pos=20000)
+    try:
+        for n, wl in enumerate([I.make_workload("na", [5000, 300, 12000], [1, 1, 1], [1, 1, 1], True, 512,
+                                                seed=41, wid=40),
+                                I.make_workload("nb", [2500, 700], [8, 8], [2500, 700], True, 1024,
+                                                seed=42, wid=41)]):
+            d = U.device_workload(wl, fmt, ctx)
+            ref_i, ref_s = U.run_topk(wl, fmt, ctx, d)
+            for call in range(2):   # two calls in a row share the static scratch
+                out_i = torch.full((wl.Tq, wl.k), 7, dtype=torch.int32, device="cuda")
+                out_s = torch.full((wl.Tq, wl.k), 7.0, dtype=torch.float32, device="cuda")
+                st = _call_static(ctx, wl, fmt, d, wl.k, out_i, out_s)
+                assert st == 0, f"workload {n} call {call}: status {st}"
+                torch.cuda.synchronize()
+                assert ctx.device_status() == 0
+                gi, gs = out_i.cpu().numpy(), out_s.cpu().numpy()
+                # same kernels and inputs: positions equal, scores within the bf16 logit tolerance
+                assert np.array_equal(gi, ref_i), f"workload {n} call {call}: positions differ"
+                fin = np.isfinite(ref_s)
+                assert np.array_equal(fin, np.isfinite(gs))
+                assert np.allclose(gs[fin], ref_s[fin], rtol=2e-3, atol=0)
+    finally:
+        ctx.close()
+
+
+def test_static_scratch_rejects_oversized_request():
+    import torch
+    from dsa_sparse_attention_store_gb300 import Context
+    ctx = Context(theta=10000.0, eps=1e-6, max_pos=4096)
+    try:
+        Tq = 4096   # fp8 keeps 16.6 KB per query in the scratch: more than the fixed array holds
+        wl = I.make_workload("big", [Tq], [Tq], [0], True, 512, seed=43, wid=42)
+        d = U.device_workload(wl, 1, ctx, store_fill=False, store_new=False)
+        out_i = torch.zeros((Tq, 512), dtype=torch.int32, device="cuda")
+        out_s = torch.zeros((Tq, 512), dtype=torch.float32, device="cuda")
+        assert _call_static(ctx, wl, 1, d, 512, out_i, out_s) == 6     # DSA_ERR_WORKSPACE
+        torch.cuda.synchronize()
+        assert int(out_i.abs().sum()) == 0                            # nothing was launched
+    finally:
+        ctx.close()
