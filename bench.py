@@ -235,8 +235,7 @@ def run_ours(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    ctx.profile_read()
-    ctx.profile_enable(True)
+    ctx.profile_read()                      # resets the launch counters
     barrier()
     sampler.mark(True)
     for i in range(args.steps):
@@ -246,10 +245,20 @@ def run_ours(args, rank, world, local_rank):
         flush()
     barrier()
     sampler.mark(False)
-    ctx.profile_enable(False)
-    prof = ctx.profile_read()
+    launches = sum(n for _, n in ctx.profile_read().values())
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = sum(step_ms)
+
+    # per-kernel times: the same steps again with the library's kernel events
+    # on (events between kernels stop programmatic dependent launch from
+    # overlapping them, so these are slightly pessimistic)
+    ctx.profile_enable(True)
+    for i in range(args.steps):
+        step(d)
+        flush()
+    torch.cuda.synchronize()
+    ctx.profile_enable(False)
+    prof = ctx.profile_read()
 
     # end-to-end through the C ABI from pinned host buffers
     e2e_ms = None
@@ -295,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
 
     # roofline of the scorer, per cache format (its launches in the timed region)
     peaks, peak_src = load_peaks()
-    launches_per_step = sum(n for _, n in prof.values()) / max(args.steps, 1)
+    launches_per_step = launches / max(args.steps, 1)
     pages = sum((int(L) + 63) // 64 for L in wl.seq_lens)
     flops_launch = wl.key_scores() * 2 * 64 * 128
 
@@ -341,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
         "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "roofline": roofs[fmts[0]],
         "roofline_other_format": roofs[fmts[1]] if len(fmts) > 1 else None,
-        "gpu_launches": int(sum(n for _, n in prof.values())),
+        "gpu_launches": int(launches),
         "launches_per_step": launches_per_step,
         "clocks": clocks,
     }

@@ -202,7 +202,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
   if (!q || !head_w || !cache || !page_table || !seq_lens || !cu_q || !out_idx || !out_score ||
       !workspace)
     return DSA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(workspace, 256) || !aligned(head_w, 4) ||
+  if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(workspace, 256) || !aligned(head_w, 16) ||
       !aligned(out_idx, 4) || !aligned(out_score, 4))
     return DSA_ERR_INVALID_ARG;
   if (ws_bytes < dsa::topk_workspace(ctx, Tq, B, k, fmt)) return DSA_ERR_WORKSPACE;

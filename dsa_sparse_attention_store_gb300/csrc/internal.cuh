@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "../../include/dsaidx.h"
 
@@ -53,6 +54,31 @@ struct LaunchScope {
     if (rec) cudaEventRecord(rec->ev1, stream);
   }
 };
+
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel on the stream is still running, so every kernel
+// launched this way executes griddepcontrol.wait before it reads global
+// memory that a predecessor may write.
+template <typename... Kargs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Kargs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 }  // namespace dsa
 
 namespace dsa {

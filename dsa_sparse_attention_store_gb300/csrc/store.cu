@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) store_kernel(
     const int32_t* __restrict__ seq_id, const int32_t* __restrict__ page_table, int T, int B,
     int max_pages, uint8_t* __restrict__ cache, int num_pages, const float2* __restrict__ rope,
     int max_pos, const float* __restrict__ gamma, float eps, unsigned int* status) {
+  pdl_wait();
+  pdl_trigger();
   const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
   const int l = threadIdx.x & 15;
   const bool live = tok < T;
@@ -146,17 +148,13 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
   const long long threads = static_cast<long long>(T) * 16;
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   LaunchScope scope(ctx, DSA_K_STORE, stream);
-  if (fmt == DSA_FMT_BF16)
-    store_kernel<DSA_FMT_BF16><<<blocks, 256, 0, stream>>>(
-        static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B, max_pages,
-        static_cast<uint8_t*>(cache), num_pages, ctx->rope, ctx->max_pos, ctx->gamma, ctx->eps,
-        ctx->status);
-  else
-    store_kernel<DSA_FMT_FP8><<<blocks, 256, 0, stream>>>(
-        static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B, max_pages,
-        static_cast<uint8_t*>(cache), num_pages, ctx->rope, ctx->max_pos, ctx->gamma, ctx->eps,
-        ctx->status);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  auto kern = fmt == DSA_FMT_BF16 ? store_kernel<DSA_FMT_BF16> : store_kernel<DSA_FMT_FP8>;
+  const cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, stream,
+                                   static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B,
+                                   max_pages, static_cast<uint8_t*>(cache), num_pages,
+                                   static_cast<const float2*>(ctx->rope), ctx->max_pos,
+                                   static_cast<const float*>(ctx->gamma), ctx->eps, ctx->status);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace dsa

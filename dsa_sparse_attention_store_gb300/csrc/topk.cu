@@ -16,9 +16,10 @@
 // (when a query tile's context is split across CTAs) and, for fp8 caches,
 // the queries converted for the tensor cores.
 //
-// Kernels, in launch order:
-//   plan    one CTA: query tiles (QT queries of one sequence) and a prefix sum
-//           of their key-tile counts, so CTAs can split the total work evenly.
+// Kernels, in launch order (all with programmatic dependent launch):
+//   plan    one CTA: query tiles (QT queries of one sequence), a prefix sum
+//           of their key-tile counts, and each CTA's first query tile, so the
+//           CTAs split the total work evenly with one dependent load.
 //   qprep   fp8 caches only: q -> f16 with a power-of-two scale per (query,
 //           head) so the largest magnitude lands in [2^14, 2^15); the scale's
 //           inverse is folded into the head weight (exact).
@@ -27,11 +28,11 @@
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
 //                         x K=128 into one of two TMEM accumulators
 //             4*NG warps  epilogue: tcgen05.ld, ReLU, head-weighted sum, mask,
-//                         threshold filter into the running top-k
+//                         threshold filter into the running top-k; at the end
+//                         of a query tile: exact selection, sort, output
 //             4 warps     (fp8) e4m3 -> f16 conversion of staged key tiles
 //           Keys sit on the MMA's M dimension so each epilogue thread owns one
 //           key (one TMEM lane) and reduces over heads in its own registers.
-//   sort    one warp per output row: bitonic sort by (score desc, pos asc).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -49,14 +50,20 @@ constexpr int kD = 128;
 constexpr int kTile = 128;  // keys per MMA tile = 2 pages
 constexpr int kPageBytesFp8 = 64 * 128 + 64 * 4;
 
+// The work is split evenly in units: a query tile with n key tiles costs
+// n + ovh units, ovh standing for its fixed costs (query load, final
+// selection and sort), so CTAs that get many short query tiles get fewer.
 struct PlanHdr {
-  int qtot;
-  int pad;
-  long long total;
+  int qtot;         // query tiles
+  int Ge;           // CTAs with work: min(grid, total units)
+  long long total;  // units over all query tiles
+  int ovh;          // units charged per query tile on top of its key tiles
 };
 
+// Per query tile: {b, row0, nrows, ntile} and {L, qpos0, 0, 0} where qpos0 is
+// the position of the tile's first query.
 struct WsLayout {
-  size_t hdr, seq_qoff, meta, prefix, counters, partials, qh, wq, total;
+  size_t hdr, seq_qoff, meta, prefix, counters, rec, partials, qh, wq, total;
   int QT, G, qtmax, NG;
 };
 
@@ -76,11 +83,13 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
   L.seq_qoff = o;
   o = up256(o + static_cast<size_t>(B + 1) * 4);
   L.meta = o;
-  o = up256(o + static_cast<size_t>(L.qtmax) * 16);
+  o = up256(o + static_cast<size_t>(L.qtmax) * 32);
   L.prefix = o;
   o = up256(o + static_cast<size_t>(L.qtmax + 1) * 8);
   L.counters = o;
   o = up256(o + static_cast<size_t>(L.qtmax) * L.NG * 4);
+  L.rec = o;
+  o = up256(o + static_cast<size_t>(L.G) * 4);
   L.partials = o;
   o = up256(o + static_cast<size_t>(2) * L.G * L.QT * k * 8);
   if (fmt == DSA_FMT_FP8) {
@@ -139,19 +148,26 @@ __device__ T block_excl_scan(T v, T* sm, T& total) {
   return excl;
 }
 
+__device__ __forceinline__ long long range_start(int c, long long total, int G) {
+  return static_cast<long long>(c) * total / G;
+}
+
 // ------------------------------------------------------------------ plan
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ cu_q, int B, int Tq,
                                                     int QT, int NG, int causal, int max_pages, int k,
-                                                    char* ws, WsLayout L, int32_t* out_idx,
+                                                    int ovh, char* ws, WsLayout L, int32_t* out_idx,
                                                     float* out_score, unsigned int* status) {
   __shared__ int smi[32];
   __shared__ long long sml[32];
+  pdl_wait();
+  pdl_trigger();
   PlanHdr* hdr = reinterpret_cast<PlanHdr*>(ws + L.hdr);
   int* qoff = reinterpret_cast<int*>(ws + L.seq_qoff);
   int4* meta = reinterpret_cast<int4*>(ws + L.meta);
   long long* prefix = reinterpret_cast<long long*>(ws + L.prefix);
   int* cnt = reinterpret_cast<int*>(ws + L.counters);
+  int* rec = reinterpret_cast<int*>(ws + L.rec);
 
   int carry = 0;
   for (int base = 0; base < B; base += 1024) {
@@ -190,11 +206,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       const int q0 = cu_q[b], nq = cu_q[b + 1] - q0, Ls = seq_lens[b];
       const int row0 = q0 + t * QT;
       const int nrows = min(QT, nq - t * QT);
-      const int kend = causal ? (Ls - nq + t * QT + nrows) : Ls;
+      const int qpos0 = Ls - nq + t * QT;
+      const int kend = causal ? (qpos0 + nrows) : Ls;
       const int ntile = kend > 0 ? (kend + kTile - 1) / kTile : 0;
       m = make_int4(b, row0, nrows, ntile);
-      meta[qt] = m;
-      cost = ntile;
+      meta[2 * qt] = m;
+      meta[2 * qt + 1] = make_int4(Ls, qpos0, 0, 0);
+      cost = ntile > 0 ? ntile + ovh : 0;
     }
     long long tot;
     const long long ex = block_excl_scan<long long>(cost, sml, tot);
@@ -211,10 +229,27 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
     lcarry += tot;
   }
+  const long long total = lcarry;
+  const int Ge = total < L.G ? static_cast<int>(total) : L.G;
   if (threadIdx.x == 0) {
-    prefix[qtot] = lcarry;
+    prefix[qtot] = total;
     hdr->qtot = qtot;
-    hdr->total = lcarry;
+    hdr->Ge = Ge;
+    hdr->total = total;
+    hdr->ovh = ovh;
+  }
+  __syncthreads();
+  // first query tile of each CTA: the non-empty tile holding its range start
+  for (int qt = threadIdx.x; qt < qtot; qt += 1024) {
+    const long long p0 = prefix[qt], p1 = prefix[qt + 1];
+    if (p1 <= p0) continue;
+    int c = static_cast<int>(p0 * Ge / total);
+    while (c > 0 && range_start(c, total, Ge) >= p0) --c;
+    for (; c < Ge; ++c) {
+      const long long s = range_start(c, total, Ge);
+      if (s >= p1) break;
+      if (s >= p0) rec[c] = qt;
+    }
   }
 }
 
@@ -227,6 +262,8 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
                                                     const float* __restrict__ w,
                                                     uint2* __restrict__ qh, float* __restrict__ wq,
                                                     long long rows) {
+  pdl_wait();
+  pdl_trigger();
   const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -260,7 +297,9 @@ struct Cfg {
   static constexpr int QPG = QT / NG;                    // queries per group
   static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 2) : (FMT == DSA_FMT_BF16 ? 5 : 2);
   static constexpr int SS = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // e4m3 staging
-  static constexpr int CAP = QT == 4 ? KSEL + 512 : 4 * KSEL;  // running top-k capacity
+  // running top-k capacity: what shared memory leaves for QT = 4; for QT = 1
+  // small enough that a compaction fits in the time the key ring covers
+  static constexpr int CAP = QT == 4 ? 1792 : (KSEL == 512 ? 1280 : 2048);
   static constexpr int NEPI = 4 * NG;
   static constexpr int NCONV = FMT == DSA_FMT_FP8 ? 4 : 0;
   static constexpr int NWARPS = 2 + NEPI + NCONV;
@@ -274,31 +313,30 @@ struct Cfg {
   static constexpr int OFF_STG = OFF_OP + S * OP_BYTES;
   static constexpr int OFF_TOPK = OFF_STG + SS * STG_BYTES;
   static constexpr int OFF_W = OFF_TOPK + QT * CAP * 8;
-  static constexpr int OFF_HIST = OFF_W + QT * 64 * 4;
-  static constexpr int OFF_MISC = OFF_HIST + NG * 256 * 4;
+  static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;  // head weights, double-buffered
+  static constexpr int OFF_MISC = OFF_HIST + NG * 512 * 4;  // per-warp packed histograms
   static constexpr int MISC_BYTES = 1024;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(CAP % 128 == 0, "capacity");
+  static_assert(CAP % 128 == 0 && CAP >= KSEL + 128, "capacity");
 };
 
 struct Misc {
   uint64_t op_full[8], op_empty[8], stg_full[8], stg_empty[8];
-  uint64_t tm_full[2], tm_empty[2], q_full, q_empty, fin;
+  uint64_t tm_full[2], tm_empty[2], q_full, q_empty, fin, w_full[2], w_empty[2];
   uint32_t tmem_base;
   int abort;
   int cnt[4];
   unsigned long long thr[4];
   int gok[2], glast[2], gdigit[2], gabove[2], gcd[2];
   int wsum[2][2][4];
+  unsigned long long gmin[2][4], gmax[2][4];
 };
 static_assert(sizeof(Misc) <= 1024, "misc");
 
 struct ScoreArgs {
   const int32_t* page_table;
   int max_pages;
-  const int32_t* seq_lens;
-  const int32_t* cu_q;
   int causal;
   const uint8_t* cache;
   int num_pages;
@@ -311,56 +349,66 @@ struct ScoreArgs {
 };
 
 struct Seg {
-  int qt, b, row0, nrows, ntile, t0, t1;
+  int qt, b, row0, nrows, ntile, t0, t1, L, qpos0;
+  long long qstart, qend;  // the query tile's range in the flattened work
   bool whole;
 };
 
 // Contiguous, equal share of the flattened (query tile, key tile) work.
 struct SegIter {
   long long g, gbeg, gend;
-  int qt;
+  int qt, ovh;
   const long long* prefix;
   const int4* meta;
-  __device__ void init(const long long* p, const int4* m, int qtot, long long total, int c, int G) {
+  __device__ void init(const long long* p, const int4* m, const int* rec, long long total, int c,
+                       int Ge, int ovh_units) {
     prefix = p;
     meta = m;
-    if (qtot <= 0 || total <= 0 || c >= G) {
+    ovh = ovh_units;
+    if (total <= 0 || c >= Ge) {
       g = gbeg = gend = 0;
       qt = 0;
       return;
     }
-    gbeg = static_cast<long long>(c) * total / G;
-    gend = static_cast<long long>(c + 1) * total / G;
+    gbeg = range_start(c, total, Ge);
+    gend = range_start(c + 1, total, Ge);
     g = gbeg;
-    int lo = 0, hi = qtot - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    qt = lo;
+    qt = rec[c];
   }
+  // Next query tile with key tiles inside this CTA's range. A query tile
+  // occupies units [p0, p1): ovh overhead units, then one unit per key tile.
   __device__ bool next(Seg& s) {
-    if (g >= gend) return false;
-    while (prefix[qt + 1] <= g) ++qt;
-    const int4 m = meta[qt];
-    const long long p = prefix[qt];
-    s.qt = qt;
-    s.b = m.x;
-    s.row0 = m.y;
-    s.nrows = m.z;
-    s.ntile = m.w;
-    s.t0 = static_cast<int>(g - p);
-    const long long e = min(static_cast<long long>(m.w), gend - p);
-    s.t1 = static_cast<int>(e);
-    s.whole = (s.t0 == 0 && s.t1 == m.w);
-    g = p + e;
-    return true;
+    while (g < gend) {
+      const long long p0 = prefix[qt], p1 = prefix[qt + 1];
+      if (p1 <= g) {
+        ++qt;
+        continue;
+      }
+      const long long tb = p0 + ovh;  // unit of key tile 0
+      const int4 m = meta[2 * qt];
+      const long long t0 = g > tb ? g - tb : 0;
+      const long long t1 = min(static_cast<long long>(m.w), gend - tb);
+      g = min(p1, gend);
+      if (t1 <= t0) continue;
+      const int4 m1 = meta[2 * qt + 1];
+      s.qt = qt;
+      s.b = m.x;
+      s.row0 = m.y;
+      s.nrows = m.z;
+      s.ntile = m.w;
+      s.L = m1.x;
+      s.qpos0 = m1.y;
+      s.qstart = p0;
+      s.qend = p1;
+      s.t0 = static_cast<int>(t0);
+      s.t1 = static_cast<int>(t1);
+      s.whole = (t0 == 0 && t1 == m.w);
+      return true;
+    }
+    return false;
   }
 };
 
-__device__ __forceinline__ long long range_start(int c, long long total, int G) {
-  return static_cast<long long>(c) * total / G;
-}
 __device__ __forceinline__ int owner_of(long long gtile, long long total, int G) {
   int c = static_cast<int>(gtile * G / total);
   while (c + 1 < G && range_start(c + 1, total, G) <= gtile) ++c;
@@ -385,31 +433,86 @@ __device__ __forceinline__ void push_key(bool pass, uint64_t key, uint64_t* buf,
   }
 }
 
-// Keep exactly the K largest keys of buf[0..cnt) (when cnt > K): radix select
-// of the K-th largest key one byte at a time (histogram of the next byte of
-// the keys that match the prefix so far), then a stable in-place compaction.
-// The filter threshold becomes the selected prefix minus one.
+// Keep exactly the K largest keys of buf[0..cnt) (when cnt > K). Radix
+// select of the K-th largest key: a min/max pass finds the highest bit where
+// the keys differ, then each pass histograms the next (up to) 8 bits of the
+// keys that still match the selected prefix. Each warp counts into its own
+// 256 bins (16-bit counters packed two per word, plain shared atomics, four
+// keys in flight per thread). The kept keys (those >= the prefix) are
+// compacted in place, four per thread per round. The filter threshold
+// becomes the selected prefix minus one. hist: 4 x 128 words.
 __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, int K,
                               uint32_t* hist, Misc* ms, int g, int gt, int barid) {
   const int n = *cnt;
   if (n <= K) return;
-  uint64_t prefix = 0, mask = 0;
+  const int w = gt >> 5, lane = gt & 31;
+  // ---- min / max of the keys
+  uint64_t mn = ~0ull, mx = 0ull;
+  for (int i = gt; i < n; i += 128) {
+    const uint64_t key = buf[i];
+    mn = key < mn ? key : mn;
+    mx = key > mx ? key : mx;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const uint64_t a = __shfl_xor_sync(0xffffffffu, mn, o);
+    const uint64_t b = __shfl_xor_sync(0xffffffffu, mx, o);
+    mn = a < mn ? a : mn;
+    mx = b > mx ? b : mx;
+  }
+  if (lane == 0) {
+    ms->gmin[g][w] = mn;
+    ms->gmax[g][w] = mx;
+  }
+  named_bar(barid, 128);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const uint64_t a = ms->gmin[g][x], b = ms->gmax[g][x];
+    mn = a < mn ? a : mn;
+    mx = b > mx ? b : mx;
+  }
+  // bits above hb are common to every key
+  int hb = 63 - __clzll(static_cast<long long>(mn ^ mx));
+  uint64_t mask = hb >= 63 ? 0ull : ~((2ull << hb) - 1ull);
+  uint64_t prefix = mn & mask;
   int remaining = K;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = gt; i < 256; i += 128) hist[i] = 0;
+  uint32_t* hw = hist + w * 128;
+  while (hb >= 0) {
+    const int lo = hb >= 7 ? hb - 7 : 0;
+    const int width = hb - lo + 1;
+    const uint64_t dmask = (1ull << width) - 1ull;
+    for (int i = gt; i < 512; i += 128) hist[i] = 0;
     named_bar(barid, 128);
-    for (int i = gt; i < n; i += 128) {
-      const uint64_t key = buf[i];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    for (int r0 = 0; r0 < n; r0 += 512) {
+      uint64_t kv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = r0 + e * 128 + gt;
+        kv[e] = i < n ? buf[i] : 0ull;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = r0 + e * 128 + gt;
+        if (i < n && (kv[e] & mask) == prefix) {
+          const uint32_t d = static_cast<uint32_t>((kv[e] >> lo) & dmask);
+          atomicAdd(&hw[d >> 1], (d & 1u) ? 0x10000u : 1u);
+        }
+      }
     }
     named_bar(barid, 128);
     if (gt < 32) {
+      // lane l holds bins 255-8l .. 248-8l (descending digits), summed over warps
       int c[8];
       int sum = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        c[e] = static_cast<int>(hist[255 - 8 * gt - e]);
-        sum += c[e];
+        const int bin = 255 - 8 * gt - e;
+        const int sh = (bin & 1) * 16;
+        int v = 0;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) v += static_cast<int>((hist[x * 128 + (bin >> 1)] >> sh) & 0xFFFFu);
+        c[e] = v;
+        sum += v;
       }
       int incl = sum;
 #pragma unroll
@@ -436,28 +539,43 @@ __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, 
     const int d = ms->gdigit[g];
     remaining -= ms->gabove[g];
     const int cd = ms->gcd[g];
-    prefix |= static_cast<uint64_t>(d) << shift;
-    mask |= 255ull << shift;
+    prefix |= static_cast<uint64_t>(d) << lo;
+    mask |= dmask << lo;
+    hb = lo - 1;
     if (cd == remaining) break;
   }
-  const int w = gt >> 5, lane = gt & 31;
+  // ---- keep keys >= prefix, in place (writes never pass the current round)
   int base = 0;
-  for (int r0 = 0; r0 < n; r0 += 128) {
-    const int i = r0 + gt;
-    const uint64_t key = i < n ? buf[i] : 0ull;
-    const bool keep = i < n && key >= prefix;
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    const int par = (r0 >> 7) & 1;
-    if (lane == 0) ms->wsum[g][par][w] = __popc(m);
+  for (int r0 = 0; r0 < n; r0 += 512) {
+    uint64_t kv[4];
+    int keep = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = r0 + e * 128 + gt;
+      kv[e] = i < n ? buf[i] : 0ull;
+      keep += (i < n && kv[e] >= prefix) ? 1 : 0;
+    }
+    int incl = keep;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int par = (r0 >> 9) & 1;
+    if (lane == 31) ms->wsum[g][par][w] = incl;
     named_bar(barid, 128);
-    int off = base, tot = 0;
+    int off = base + incl - keep, tot = 0;
 #pragma unroll
     for (int x = 0; x < 4; ++x) {
       const int v = ms->wsum[g][par][x];
       if (x < w) off += v;
       tot += v;
     }
-    if (keep) buf[off + __popc(m & ((1u << lane) - 1u))] = key;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = r0 + e * 128 + gt;
+      if (i < n && kv[e] >= prefix) buf[off++] = kv[e];
+    }
     base += tot;
   }
   named_bar(barid, 128);
@@ -466,6 +584,126 @@ __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, 
     *thr = prefix > 0 ? prefix - 1 : 0;
   }
   named_bar(barid, 128);
+}
+
+// Bitonic sorting network over K slots held by one group of 128 threads:
+// warp w owns slots [w*K/4, (w+1)*K/4); slot x = w*K/4 + e*32 + lane is
+// v[e] of that lane. Strides below 32 use shuffles, strides inside a warp's
+// quarter compare two registers of one lane, strides that cross warps go
+// through the shared-memory array xbuf (K slots). Descending where
+// (x & size) == 0.
+template <int K>
+__device__ __forceinline__ void bitonic_stage(uint64_t (&v)[K / 128], int size, int stride,
+                                              uint64_t* xbuf, int w, int lane, int barid) {
+  constexpr int PW = K / 4;
+  constexpr int E = PW / 32;
+  if (stride >= PW) {
+    named_bar(barid, 128);
+#pragma unroll
+    for (int e = 0; e < E; ++e) xbuf[w * PW + e * 32 + lane] = v[e];
+    named_bar(barid, 128);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int x = w * PW + e * 32 + lane;
+      const uint64_t o = xbuf[x ^ stride];
+      const bool lower = (x & stride) == 0;
+      const bool desc = (x & size) == 0;
+      const uint64_t mx = v[e] > o ? v[e] : o;
+      const uint64_t mn = v[e] > o ? o : v[e];
+      v[e] = (lower == desc) ? mx : mn;
+    }
+  } else if (stride >= 32) {
+    const int je = stride >> 5;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int e2 = e ^ je;
+      if (e2 > e) {
+        const int x = w * PW + e * 32 + lane;
+        const bool desc = (x & size) == 0;
+        const uint64_t a = v[e], b = v[e2];
+        const bool sw = desc ? (a < b) : (a > b);
+        v[e] = sw ? b : a;
+        v[e2] = sw ? a : b;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int x = w * PW + e * 32 + lane;
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], stride);
+      const bool lower = (lane & stride) == 0;
+      const bool desc = (x & size) == 0;
+      const uint64_t mx = v[e] > o ? v[e] : o;
+      const uint64_t mn = v[e] > o ? o : v[e];
+      v[e] = (lower == desc) ? mx : mn;
+    }
+  }
+}
+
+// Sort buf[0..n) (n <= K, distinct keys) descending into registers; slots
+// past n hold 0 (below every key).
+template <int K>
+__device__ void group_sort_regs(uint64_t* buf, int n, uint64_t (&v)[K / 128], int gt, int barid) {
+  constexpr int PW = K / 4;
+  constexpr int E = PW / 32;
+  const int w = gt >> 5, lane = gt & 31;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int x = w * PW + e * 32 + lane;
+    v[e] = x < n ? buf[x] : 0ull;
+  }
+#pragma unroll
+  for (int size = 2; size <= K; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, size, stride, buf, w, lane, barid);
+  }
+  named_bar(barid, 128);
+}
+
+// v (sorted descending) := the K largest of v and another descending list
+// src (K keys, global memory), sorted descending: the elementwise max of v and
+// src reversed is a bitonic sequence holding the K largest, and one bitonic
+// merge sorts it.
+template <int K>
+__device__ void group_merge_regs(uint64_t (&v)[K / 128], const unsigned long long* src,
+                                 uint64_t* xbuf, int gt, int barid) {
+  constexpr int PW = K / 4;
+  constexpr int E = PW / 32;
+  const int w = gt >> 5, lane = gt & 31;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int x = w * PW + e * 32 + lane;
+    const uint64_t o = __ldcg(src + (K - 1 - x));
+    v[e] = v[e] > o ? v[e] : o;
+  }
+#pragma unroll
+  for (int stride = K >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
+  named_bar(barid, 128);
+}
+
+// Write one output row from sorted registers: positions and scores, -1 / -inf
+// for empty slots.
+template <int K>
+__device__ __forceinline__ void write_row(const uint64_t (&v)[K / 128], int32_t* oi, float* os, int gt) {
+  constexpr int PW = K / 4;
+  constexpr int E = PW / 32;
+  const int w = gt >> 5, lane = gt & 31;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int x = w * PW + e * 32 + lane;
+    const uint64_t key = v[e];
+    oi[x] = key ? key_pos(key) : -1;
+    os[x] = key ? key_score(key) : -__int_as_float(0x7f800000);
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void write_keys(const uint64_t (&v)[K / 128], unsigned long long* dst, int gt) {
+  constexpr int PW = K / 4;
+  constexpr int E = PW / 32;
+  const int w = gt >> 5, lane = gt & 31;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[w * PW + e * 32 + lane] = v[e];
 }
 
 // ------------------------------------------------------------------ the scorer
@@ -485,7 +723,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
   Misc* ms = reinterpret_cast<Misc*>(sm + C::OFF_MISC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x, cta = blockIdx.x;
+  const int cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
@@ -502,6 +740,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     }
     mbar_init(&ms->q_full, 1);
     mbar_init(&ms->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ms->w_full[i], 1);
+      mbar_init(&ms->w_empty[i], C::NG);
+    }
     mbar_init(&ms->fin, 1);
     ms->abort = 0;
     fence_mbar_init();
@@ -519,16 +761,19 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
   tc_fence_after();
   const uint32_t tbase = ms->tmem_base;
 
+  // everything above is local set-up; global inputs are read only after the
+  // previous kernel on the stream has completed
+  pdl_wait();
+  pdl_trigger();
   const PlanHdr* hdr = reinterpret_cast<const PlanHdr*>(a.ws + a.L.hdr);
   const int4* meta = reinterpret_cast<const int4*>(a.ws + a.L.meta);
   const long long* prefix = reinterpret_cast<const long long*>(a.ws + a.L.prefix);
-  const int qtot = hdr->qtot;
+  const int* rec = reinterpret_cast<const int*>(a.ws + a.L.rec);
   const long long total = hdr->total;
-  // CTAs c < Ge get non-empty, contiguous ranges of the flattened work;
-  // with Ge <= total every such range holds at least one tile.
-  const int Ge = total < G ? static_cast<int>(total) : G;
+  const int Ge = hdr->Ge;
+  const int ovh = hdr->ovh;
   SegIter it;
-  it.init(prefix, meta, qtot, total, cta, Ge);
+  it.init(prefix, meta, rec, total, cta, Ge, ovh);
   volatile int* abort_flag = &ms->abort;
 
   if (warp == 0) {
@@ -537,9 +782,16 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     Seg s;
     bool stop = false;
     while (!stop && it.next(s)) {
-      const int Ls = a.seq_lens[s.b];
-      const int npg = (Ls + 63) >> 6;
+      const int npg = (s.L + 63) >> 6;
       const int32_t* pt = a.page_table + static_cast<long long>(s.b) * a.max_pages;
+      int pid0 = -1, pid1 = -1;
+      {  // page ids of the first 32 tiles, before waiting for the Q buffer
+        const int tt = s.t0 + lane;
+        if (tt < s.t1) {
+          if (2 * tt < npg) pid0 = pt[2 * tt];
+          if (2 * tt + 1 < npg) pid1 = pt[2 * tt + 1];
+        }
+      }
       if (lane == 0) {
         if (!mbar_wait(&ms->q_empty, (seg_i & 1) ^ 1)) {
           atomicOr(a.status, DSA_DEV_TIMEOUT);
@@ -549,15 +801,28 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
           tma_load_2d(sQ + C::N * 128, &tm_q, 64, s.row0 * kH, &ms->q_full);
         }
+        // the tile's head-weight rows into the weight buffer the epilogue
+        // released two query tiles ago (each buffer has its own barriers, so
+        // the producer can never run two tiles ahead of the epilogue on it)
+        const int wb = seg_i & 1, wu = seg_i >> 1;
+        if (!*abort_flag) {
+          if (!mbar_wait(&ms->w_empty[wb], (wu & 1) ^ 1)) {
+            atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          } else {
+            mbar_arrive_expect_tx(&ms->w_full[wb], s.nrows * kH * 4);
+            bulk_load(sW + wb * (QT * 64), a.w + static_cast<long long>(s.row0) * kH,
+                      s.nrows * kH * 4, &ms->w_full[wb]);
+          }
+        }
       }
-      int pid0 = -1, pid1 = -1;
       for (int t = s.t0; t < s.t1; ++t) {
         if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
           stop = true;
           break;
         }
         const int rel = (t - s.t0) & 31;
-        if (rel == 0) {
+        if (rel == 0 && t > s.t0) {
           const int tt = t + lane;
           pid0 = -1;
           pid1 = -1;
@@ -615,7 +880,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         mbar_wait(fb, (ts / R) & 1, 20000000LL);
       }
       mbar_wait(&ms->q_full, (seg_i - 1) & 1, 20000000LL);
+      if (seg_i > 0) mbar_wait(&ms->w_full[(seg_i - 1) & 1], ((seg_i - 1) >> 1) & 1, 20000000LL);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -661,6 +928,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       tc_commit(&ms->fin);
       mbar_wait(&ms->fin, 0, 200000000LL);
     }
+    __syncwarp();
   } else if (warp < 2 + C::NEPI) {
     // ---------------------------------------------------------- epilogue
     const int g = (warp - 2) >> 2;
@@ -668,19 +936,17 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const int barid = 1 + g;
-    uint32_t* hist = sHist + g * 256;
+    uint32_t* hist = sHist + g * 512;
     int tile_seq = 0;
     Seg s;
     bool stop = false;
-    const long long qt_stride = C::NG;
     int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
     unsigned long long* partials =
         reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
+    int seg_i = 0;
     while (!stop && it.next(s)) {
-      const int Ls = a.seq_lens[s.b];
-      const int cq = a.cu_q[s.b];
-      const int nq = a.cu_q[s.b + 1] - cq;
       const int32_t* pt = a.page_table + static_cast<long long>(s.b) * a.max_pages;
+      const float* sWs = sW + (seg_i & 1) * (QT * 64);
       int lim[C::QPG];
       unsigned long long thr[C::QPG];
 #pragma unroll
@@ -690,15 +956,23 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           ms->cnt[j] = 0;
           ms->thr[j] = 0;
         }
-        if (gt < 64) sW[j * 64 + gt] = j < s.nrows ? a.w[static_cast<long long>(s.row0 + j) * kH + gt] : 0.f;
-        lim[jj] = j < s.nrows ? (a.causal ? (Ls - nq + (s.row0 - cq) + j + 1) : Ls) : 0;
+        lim[jj] = j < s.nrows ? (a.causal ? s.qpos0 + j + 1 : s.L) : 0;
         thr[jj] = 0;
       }
+      // the producer loads this tile's head weights into buffer seg_i & 1
+      if (gt == 0) ms->gok[g] = mbar_wait(&ms->w_full[seg_i & 1], (seg_i >> 1) & 1) && !*abort_flag;
       named_bar(barid, 128);
+      if (!ms->gok[g]) {
+        if (gt == 0) {
+          atomicOr(a.status, DSA_DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
       for (int t = s.t0; t < s.t1; ++t) {
         const int pos = t * kTile + row;
         int pid = -1;
-        if (pos < Ls) {
+        if (pos < s.L) {
           pid = pt[pos >> 6];
           if (pid < 0 || pid >= a.num_pages) pid = -1;
         }
@@ -720,32 +994,38 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           break;
         }
         tc_fence_after();
+        {
+          const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) +
+                              static_cast<uint32_t>(buf * C::N + g * C::QPG * 64);
+          float va[64], vb[64];
+          tmem_ld64(tl, va);
+          tmem_ld_wait();
 #pragma unroll
-        for (int jj = 0; jj < C::QPG; ++jj) {
-          const int j = g * C::QPG + jj;
-          const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) +
-                                 static_cast<uint32_t>(buf * C::N + j * 64);
-          const float4* w4 = reinterpret_cast<const float4*>(sW + j * 64);
-          float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-          float v[32];
+          for (int jj = 0; jj < C::QPG; ++jj) {
+            const int j = g * C::QPG + jj;
+            // the next query's accumulators load while this one is reduced
+            if (jj + 1 < C::QPG) tmem_ld64(tl + (jj + 1) * 64, (jj & 1) ? va : vb);
+            const float* v = (jj & 1) ? vb : va;
+            const float4* w4 = reinterpret_cast<const float4*>(sWs + j * 64);
+            float acc[8];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            tmem_ld32(taddr + half * 32, v);
-            tmem_ld_wait();
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
-              const float4 ww = w4[half * 8 + h4];
-              acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
-              acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
-              acc2 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc2);
-              acc3 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc3);
+            for (int h4 = 0; h4 < 16; ++h4) {
+              const float4 ww = w4[h4];
+              const int b = (h4 & 1) * 4;
+              acc[b + 0] = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc[b + 0]);
+              acc[b + 1] = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc[b + 1]);
+              acc[b + 2] = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc[b + 2]);
+              acc[b + 3] = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc[b + 3]);
             }
+            float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
+            const uint64_t key = make_key(sc, pos);
+            const bool pass = pid >= 0 && pos < lim[jj] && key > thr[jj];
+            push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
+            if (jj + 1 < C::QPG) tmem_ld_wait();
           }
-          float sc = (acc0 + acc1) + (acc2 + acc3);
-          if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
-          const uint64_t key = make_key(sc, pos);
-          const bool pass = pid >= 0 && pos < lim[jj] && key > thr[jj];
-          push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
         }
         tc_fence_before();
         __syncwarp();
@@ -769,84 +1049,60 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           const int j = g * C::QPG + jj;
           group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
           if (j < s.nrows) {
-            const int n = min(ms->cnt[j], KSEL);
             const long long o = static_cast<long long>(s.row0 + j) * KSEL;
-            for (int i = gt; i < KSEL; i += 128) {
-              if (i < n) {
-                const uint64_t key = sTopk[j * C::CAP + i];
-                a.out_idx[o + i] = key_pos(key);
-                a.out_score[o + i] = key_score(key);
-              } else {
-                a.out_idx[o + i] = -1;
-                a.out_score[o + i] = -__int_as_float(0x7f800000);
-              }
-            }
+            uint64_t v[KSEL / 128];
+            group_sort_regs<KSEL>(sTopk + j * C::CAP, min(ms->cnt[j], KSEL), v, gt, barid);
+            write_row<KSEL>(v, a.out_idx + o, a.out_score + o, gt);
           }
         }
       } else {
-        const long long qstart = prefix[s.qt];
-        const int slot = partial_slot(cta, qstart, total, Ge);
+        // this CTA holds one piece of the query tile's keys: publish its
+        // sorted top-k; the last piece to finish merges all of them
+        const int slot = partial_slot(cta, s.qstart, total, Ge);
 #pragma unroll
         for (int jj = 0; jj < C::QPG; ++jj) {
           const int j = g * C::QPG + jj;
           group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
-          const int n = min(ms->cnt[j], KSEL);
-          unsigned long long* dst = partials + (static_cast<long long>(slot) * QT + j) * KSEL;
-          for (int i = gt; i < KSEL; i += 128) dst[i] = i < n ? sTopk[j * C::CAP + i] : 0ull;
+          if (j < s.nrows) {
+            uint64_t v[KSEL / 128];
+            group_sort_regs<KSEL>(sTopk + j * C::CAP, min(ms->cnt[j], KSEL), v, gt, barid);
+            write_keys<KSEL>(v, partials + (static_cast<long long>(slot) * QT + j) * KSEL, gt);
+          }
         }
         __threadfence();
         named_bar(barid, 128);
-        const int cf = owner_of(qstart, total, Ge);
-        const int cl = owner_of(prefix[s.qt + 1] - 1, total, Ge);
+        const int cf = owner_of(s.qstart + ovh, total, Ge);  // owner of key tile 0
+        const int cl = owner_of(s.qend - 1, total, Ge);
         if (gt == 0) {
-          const int old = atomicAdd(&counters[s.qt * qt_stride + g], 1);
+          const int old = atomicAdd(&counters[s.qt * C::NG + g], 1);
           ms->glast[g] = (old == cl - cf);
           __threadfence();
         }
         named_bar(barid, 128);
         if (ms->glast[g]) {
-          // last piece of this query tile: merge every CTA's partial list
 #pragma unroll
           for (int jj = 0; jj < C::QPG; ++jj) {
             const int j = g * C::QPG + jj;
-            if (gt == 0) {
-              ms->cnt[j] = 0;
-              ms->thr[j] = 0;
-            }
-            named_bar(barid, 128);
-            unsigned long long th = 0;
-            for (int c = cf; c <= cl; ++c) {
-              const int sl = partial_slot(c, qstart, total, Ge);
-              const unsigned long long* src = partials + (static_cast<long long>(sl) * QT + j) * KSEL;
-              for (int r0 = 0; r0 < KSEL; r0 += 128) {
-                const unsigned long long key = __ldcg(src + r0 + gt);
-                push_key(key > th, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
-                named_bar(barid, 128);
-                if (ms->cnt[j] > C::CAP - kTile)
-                  group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
-                th = ms->thr[j];
-                named_bar(barid, 128);  // every thread has read cnt before the next pushes
-              }
-            }
-            group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
             if (j < s.nrows) {
-              const int n = min(ms->cnt[j], KSEL);
-              const long long o = static_cast<long long>(s.row0 + j) * KSEL;
-              for (int i = gt; i < KSEL; i += 128) {
-                if (i < n) {
-                  const uint64_t key = sTopk[j * C::CAP + i];
-                  a.out_idx[o + i] = key_pos(key);
-                  a.out_score[o + i] = key_score(key);
-                } else {
-                  a.out_idx[o + i] = -1;
-                  a.out_score[o + i] = -__int_as_float(0x7f800000);
-                }
+              uint64_t v[KSEL / 128];
+              const unsigned long long* src0 =
+                  partials + (static_cast<long long>(partial_slot(cf, s.qstart, total, Ge)) * QT + j) * KSEL;
+#pragma unroll
+              for (int e = 0; e < KSEL / 128; ++e) v[e] = __ldcg(src0 + (gt >> 5) * (KSEL / 4) + e * 32 + lane);
+              for (int c = cf + 1; c <= cl; ++c) {
+                const unsigned long long* src =
+                    partials + (static_cast<long long>(partial_slot(c, s.qstart, total, Ge)) * QT + j) * KSEL;
+                group_merge_regs<KSEL>(v, src, sTopk + j * C::CAP, gt, barid);
               }
+              const long long o = static_cast<long long>(s.row0 + j) * KSEL;
+              write_row<KSEL>(v, a.out_idx + o, a.out_score + o, gt);
             }
           }
         }
       }
       named_bar(barid, 128);
+      if (gt == 0) mbar_arrive(&ms->w_empty[seg_i & 1]);  // this group is done with the weights
+      ++seg_i;
     }
   } else {
     // ---------------------------------------------------------- fp8: e4m3 -> f16 converters
@@ -913,60 +1169,6 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
   }
 }
 
-// ------------------------------------------------------------------ row sort
-template <int K>
-__global__ void __launch_bounds__(256) sort_rows_kernel(int32_t* __restrict__ out_idx,
-                                                        float* __restrict__ out_score, int rows) {
-  constexpr int E = K / 32;
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  int32_t* oi = out_idx + static_cast<long long>(r) * K;
-  float* os = out_score + static_cast<long long>(r) * K;
-  uint64_t v[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int idx = oi[e * 32 + lane];
-    v[e] = idx >= 0 ? make_key(os[e * 32 + lane], idx) : 0ull;
-  }
-#pragma unroll
-  for (int kk = 2; kk <= K; kk <<= 1) {
-#pragma unroll
-    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-      if (jj >= 32) {
-        const int je = jj >> 5;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int e2 = e ^ je;
-          if (e2 > e) {
-            const bool desc = ((e * 32) & kk) == 0;
-            const uint64_t x = v[e], y = v[e2];
-            const bool sw = desc ? (x < y) : (x > y);
-            v[e] = sw ? y : x;
-            v[e2] = sw ? x : y;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], jj);
-          const bool lower = (lane & jj) == 0;
-          const bool desc = ((e * 32 + lane) & kk) == 0;
-          const uint64_t mx = v[e] > o ? v[e] : o;
-          const uint64_t mn = v[e] > o ? o : v[e];
-          v[e] = (lower == desc) ? mx : mn;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const uint64_t key = v[e];
-    oi[e * 32 + lane] = key ? key_pos(key) : -1;
-    os[e * 32 + lane] = key ? key_score(key) : -__int_as_float(0x7f800000);
-  }
-}
-
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -981,8 +1183,8 @@ dsa_status run_score(dsa_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return DSA_ERR_CUDA;
   LaunchScope scope(ctx, FMT == DSA_FMT_BF16 ? DSA_K_SCORE_BF16 : DSA_K_SCORE_FP8, stream);
-  kern<<<G, C::NTHREADS, C::SMEM, stream>>>(tq, tk, args);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(kern, dim3(G), dim3(C::NTHREADS), C::SMEM, stream, tq, tk, args);
+  return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 template <int QT, int FMT>
@@ -1008,23 +1210,22 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   char* ws = static_cast<char*>(workspace);
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
-    plan_kernel<<<1, 1024, 0, stream>>>(seq_lens, cu_q, B, Tq, L.QT, L.NG, causal, max_pages, k, ws,
-                                        L, out_idx, out_score, ctx->status);
+    const int ovh = L.QT == 4 ? 12 : 4;  // measured fixed cost of a query tile, in key tiles
+    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, seq_lens, cu_q, B, Tq, L.QT, L.NG,
+                   causal, max_pages, k, ovh, ws, L, out_idx, out_score, ctx->status) != cudaSuccess)
+      return DSA_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
 
   const void* qsrc = q;
   const float* wsrc = head_w;
   const long long rows = static_cast<long long>(Tq) * kH;
   if (fmt == DSA_FMT_FP8) {
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
-    {
-      LaunchScope scope(ctx, DSA_K_QPREP, stream);
-      qprep_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint2*>(q), head_w,
-                                               reinterpret_cast<uint2*>(ws + L.qh),
-                                               reinterpret_cast<float*>(ws + L.wq), rows);
-    }
-    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+    LaunchScope scope(ctx, DSA_K_QPREP, stream);
+    if (launch_pdl(qprep_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const uint2*>(q),
+                   head_w, reinterpret_cast<uint2*>(ws + L.qh), reinterpret_cast<float*>(ws + L.wq),
+                   rows) != cudaSuccess)
+      return DSA_ERR_CUDA;
     qsrc = ws + L.qh;
     wsrc = reinterpret_cast<const float*>(ws + L.wq);
   }
@@ -1065,8 +1266,6 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   ScoreArgs args;
   args.page_table = page_table;
   args.max_pages = max_pages;
-  args.seq_lens = seq_lens;
-  args.cu_q = cu_q;
   args.causal = causal;
   args.cache = static_cast<const uint8_t*>(cache);
   args.num_pages = num_pages;
@@ -1077,22 +1276,11 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   args.out_score = out_score;
   args.status = ctx->status;
   const int G = L.G;
-  dsa_status st;
   if (L.QT == 4)
-    st = fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
-                             : run_score_k<4, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
-  else
-    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
+    return fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
+                               : run_score_k<4, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
+  return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
                              : run_score_k<1, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
-  if (st != DSA_OK) return st;
-
-  const unsigned sblocks = static_cast<unsigned>((Tq + 7) / 8);
-  LaunchScope scope(ctx, DSA_K_SORT, stream);
-  if (k == 512)
-    sort_rows_kernel<512><<<sblocks, 256, 0, stream>>>(out_idx, out_score, Tq);
-  else
-    sort_rows_kernel<1024><<<sblocks, 256, 0, stream>>>(out_idx, out_score, Tq);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace dsa

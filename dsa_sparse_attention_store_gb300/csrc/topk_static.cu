@@ -68,7 +68,7 @@ extern "C" dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const f
   if (!q || !head_w || !cache || !page_table || !seq_lens || !cu_q || !out_idx || !out_score)
     return DSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(cache) & 255) ||
-      !aligned4(head_w) || !aligned4(out_idx) || !aligned4(out_score))
+      (reinterpret_cast<uintptr_t>(head_w) & 15) || !aligned4(out_idx) || !aligned4(out_score))
     return DSA_ERR_INVALID_ARG;
   // the sizes must fit the fixed scratch array; nothing is allocated instead
   if (dsa::topk_workspace(ctx, Tq, B, k, fmt) > static_cast<size_t>(DSA_STATIC_WORKSPACE_BYTES))

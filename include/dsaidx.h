@@ -126,7 +126,7 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  * the min(k, visible) best keys, ordered by (score desc, position asc);
  * unused slots are -1 / -inf.
  *  q           (device) [Tq][64][128] bf16, 16-byte aligned.
- *  head_w      (device) [Tq][64] fp32.
+ *  head_w      (device) [Tq][64] fp32, 16-byte aligned.
  *  cache       (device) as written by dsa_index_store, num_pages pages of fmt.
  *  page_table  (device) [B][max_pages] int32; entries past a sequence's last
  *              page are not read.
