@@ -74,7 +74,7 @@ inline int pick_qt(int Tq, int B) { return (Tq >= 2 * B && Tq >= 4) ? 4 : 1; }
 WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
   WsLayout L{};
   L.QT = pick_qt(Tq, B);
-  L.NG = L.QT == 4 ? 2 : 1;
+  L.NG = L.QT;  // one epilogue group per query of the tile
   L.G = num_sms;
   L.qtmax = (Tq + L.QT - 1) / L.QT + B;
   size_t o = 0;
@@ -293,15 +293,15 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
 template <int QT, int FMT, int KSEL>
 struct Cfg {
   static constexpr int N = 64 * QT;                      // MMA N: queries x heads
-  static constexpr int NG = QT == 4 ? 2 : 1;             // epilogue groups of 4 warps
+  static constexpr int NG = QT;                          // epilogue groups of 4 warps, one per query
   static constexpr int QPG = QT / NG;                    // queries per group
   static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 2) : (FMT == DSA_FMT_BF16 ? 5 : 2);
   static constexpr int SS = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // e4m3 staging
   // running top-k capacity: what shared memory leaves for QT = 4; for QT = 1
   // small enough that a compaction fits in the time the key ring covers
-  static constexpr int CAP = QT == 4 ? 1792 : (KSEL == 512 ? 1280 : 2048);
+  static constexpr int CAP = QT == 4 ? 1536 : (KSEL == 512 ? 1280 : 2048);
   static constexpr int NEPI = 4 * NG;
-  static constexpr int NCONV = FMT == DSA_FMT_FP8 ? 4 : 0;
+  static constexpr int NCONV = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // converter warps
   static constexpr int NWARPS = 2 + NEPI + NCONV;
   static constexpr int NTHREADS = 32 * NWARPS;
   static constexpr int TMEM_COLS = 2 * N;
@@ -328,9 +328,9 @@ struct Misc {
   int abort;
   int cnt[4];
   unsigned long long thr[4];
-  int gok[2], glast[2], gdigit[2], gabove[2], gcd[2];
-  int wsum[2][2][4];
-  unsigned long long gmin[2][4], gmax[2][4];
+  int gok[4], glast[4], gdigit[4], gabove[4], gcd[4];
+  int wsum[4][2][4];
+  unsigned long long gmin[4][4], gmax[4][4];
 };
 static_assert(sizeof(Misc) <= 1024, "misc");
 
@@ -727,12 +727,12 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
-      mbar_init(&ms->op_full[i], FMT == DSA_FMT_BF16 ? 1 : 4);
+      mbar_init(&ms->op_full[i], FMT == DSA_FMT_BF16 ? 1 : C::NCONV);
       mbar_init(&ms->op_empty[i], 1);
     }
     for (int i = 0; i < C::SS; ++i) {
       mbar_init(&ms->stg_full[i], 1);
-      mbar_init(&ms->stg_empty[i], 4);
+      mbar_init(&ms->stg_empty[i], C::NCONV);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->tm_full[i], 1);
@@ -1128,8 +1128,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           const uint8_t* src = sStg + ss * C::STG_BYTES;
           uint8_t* dst = sOp + slot * C::OP_BYTES;
 #pragma unroll 2
-          for (int itn = 0; itn < 8; ++itn) {
-            const int idx = itn * 128 + ct;
+          for (int itn = 0; itn < 1024 / (32 * C::NCONV); ++itn) {
+            const int idx = itn * (32 * C::NCONV) + ct;
             const int r = idx >> 3, cb = idx & 7;
             const uint4 e = *reinterpret_cast<const uint4*>(src + r * 128 + cb * 16);
             const uint32_t wv[4] = {e.x, e.y, e.z, e.w};
