@@ -30,11 +30,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+  // the suspend-time hint (ns) lets a waiting thread sleep until the phase
+  // completes instead of re-polling, which saves issue slots for other warps
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
@@ -163,6 +165,19 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Wait for this thread's outstanding tcgen05.ld and tie the wait to the
+// destination registers, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait_regs(float (&v)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+        "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
+        "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
+        "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+      :
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -188,6 +203,20 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// d = a * b + c on two fp32 lanes at once
+__device__ __forceinline__ unsigned long long ffma2(float a0, float a1, float b0, float b1,
+                                                   unsigned long long c) {
+  unsigned long long d;
+  asm("{\n .reg .b64 ta, tb;\n mov.b64 ta, {%1, %2};\n mov.b64 tb, {%3, %4};\n"
+      " fma.rn.f32x2 %0, ta, tb, %5;\n}\n"
+      : "=l"(d)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "l"(c));
+  return d;
+}
+__device__ __forceinline__ void unpack2(unsigned long long x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
 }
 
 // ---------------------------------------------------------------- named barriers

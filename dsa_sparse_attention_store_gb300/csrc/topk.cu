@@ -969,6 +969,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         }
         break;
       }
+      static_assert(C::QPG == 1, "one query per epilogue group");
+      const int j = g;
+      const float4* w4 = reinterpret_cast<const float4*>(sWs + j * 64);
       for (int t = s.t0; t < s.t1; ++t) {
         const int pos = t * kTile + row;
         int pid = -1;
@@ -983,61 +986,50 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
                 a.cache + static_cast<long long>(pid) * kPageBytesFp8 + 64 * 128 + (pos & 63) * 4));
         }
         const int buf = tile_seq & 1, ub = tile_seq >> 1;
-        if (gt == 0) ms->gok[g] = mbar_wait(&ms->tm_full[buf], ub & 1) && !*abort_flag;
-        named_bar(barid, 128);
-        if (!ms->gok[g]) {
-          if (gt == 0) {
-            atomicOr(a.status, DSA_DEV_TIMEOUT);
-            *abort_flag = 1;
-          }
-          stop = true;
-          break;
-        }
-        tc_fence_after();
-        {
+        // every thread waits for the accumulators; a warp that gives up skips
+        // the tile, and the group agrees after the tile's barrier
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&ms->tm_full[buf], ub & 1));
+        bool pass = false;
+        uint64_t key = 0;
+        if (ok) {
+          tc_fence_after();
           const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) +
-                              static_cast<uint32_t>(buf * C::N + g * C::QPG * 64);
-          float va[64], vb[64];
-          tmem_ld64(tl, va);
+                              static_cast<uint32_t>(buf * C::N + j * 64);
+          float v[64];
+          tmem_ld64(tl, v);
           tmem_ld_wait();
+          unsigned long long a2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-          for (int jj = 0; jj < C::QPG; ++jj) {
-            const int j = g * C::QPG + jj;
-            // the next query's accumulators load while this one is reduced
-            if (jj + 1 < C::QPG) tmem_ld64(tl + (jj + 1) * 64, (jj & 1) ? va : vb);
-            const float* v = (jj & 1) ? vb : va;
-            const float4* w4 = reinterpret_cast<const float4*>(sWs + j * 64);
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-            for (int h4 = 0; h4 < 16; ++h4) {
-              const float4 ww = w4[h4];
-              const int b = (h4 & 1) * 4;
-              acc[b + 0] = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc[b + 0]);
-              acc[b + 1] = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc[b + 1]);
-              acc[b + 2] = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc[b + 2]);
-              acc[b + 3] = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc[b + 3]);
-            }
-            float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-            if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
-            const uint64_t key = make_key(sc, pos);
-            const bool pass = pid >= 0 && pos < lim[jj] && key > thr[jj];
-            push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
-            if (jj + 1 < C::QPG) tmem_ld_wait();
+          for (int h4 = 0; h4 < 16; ++h4) {
+            const float4 ww = w4[h4];
+            const int b = (h4 & 1) * 2;
+            a2[b + 0] = ffma2(ww.x, ww.y, fmaxf(v[4 * h4 + 0], 0.f), fmaxf(v[4 * h4 + 1], 0.f), a2[b + 0]);
+            a2[b + 1] = ffma2(ww.z, ww.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f), a2[b + 1]);
           }
+          float acc[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) unpack2(a2[i], acc[2 * i], acc[2 * i + 1]);
+          float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+          if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
+          key = make_key(sc, pos);
+          pass = pid >= 0 && pos < lim[0] && key > thr[0];
+        } else if (lane == 0) {
+          atomicOr(a.status, DSA_DEV_TIMEOUT);
+          *abort_flag = 1;
+          ms->gok[g] = 0;
         }
+        push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ms->tm_empty[buf]);
         named_bar(barid, 128);
-#pragma unroll
-        for (int jj = 0; jj < C::QPG; ++jj) {
-          const int j = g * C::QPG + jj;
-          if (ms->cnt[j] > C::CAP - kTile)
-            group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
-          thr[jj] = ms->thr[j];
+        if (!ms->gok[g]) {
+          stop = true;
+          break;
         }
+        if (ms->cnt[j] > C::CAP - kTile)
+          group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+        thr[0] = ms->thr[j];
         ++tile_seq;
       }
       if (stop) break;
