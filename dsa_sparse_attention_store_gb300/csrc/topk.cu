@@ -74,7 +74,7 @@ inline int pick_qt(int Tq, int B) { return (Tq >= 2 * B && Tq >= 4) ? 4 : 1; }
 WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
   WsLayout L{};
   L.QT = pick_qt(Tq, B);
-  L.NG = L.QT;  // one epilogue group per query of the tile
+  L.NG = L.QT;  // top-k groups (one per query): merge counters per (query tile, group)
   L.G = num_sms;
   L.qtmax = (Tq + L.QT - 1) / L.QT + B;
   size_t o = 0;
@@ -293,46 +293,55 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
 template <int QT, int FMT, int KSEL>
 struct Cfg {
   static constexpr int N = 64 * QT;                      // MMA N: queries x heads
-  static constexpr int NG = QT;                          // epilogue groups of 4 warps, one per query
-  static constexpr int QPG = QT / NG;                    // queries per group
+  static constexpr int QSW = QT == 4 ? 2 : 1;            // queries per score warp
+  static constexpr int NSW = 4 * QT / QSW;               // score warps (4 cover the 128 lanes)
+  static constexpr int NTK = QT;                         // top-k groups of 4 warps, one per query
+  static constexpr int QPT = QT / NTK;                   // queries per top-k group
+  static constexpr int NG = NTK;
   static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 2) : (FMT == DSA_FMT_BF16 ? 5 : 2);
   static constexpr int SS = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // e4m3 staging
-  // running top-k capacity: what shared memory leaves for QT = 4; for QT = 1
-  // small enough that a compaction fits in the time the key ring covers
-  static constexpr int CAP = QT == 4 ? 1536 : (KSEL == 512 ? 1280 : 2048);
-  static constexpr int NEPI = 4 * NG;
+  static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
+  // running top-k capacity per query
+  static constexpr int CAP = QT == 4 ? 1280 : (KSEL == 512 ? 1280 : 2048);
   static constexpr int NCONV = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // converter warps
-  static constexpr int NWARPS = 2 + NEPI + NCONV;
+  static constexpr int W_SCORE = 2;                      // first score warp
+  static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
+  static constexpr int W_CONV = W_TOPK + 4 * NTK;        // first converter warp
+  static constexpr int NWARPS = W_CONV + NCONV;
   static constexpr int NTHREADS = 32 * NWARPS;
   static constexpr int TMEM_COLS = 2 * N;
   static constexpr int Q_BYTES = N * 256;
   static constexpr int OP_BYTES = kTile * 256;
   static constexpr int STG_BYTES = kTile * 128;
+  static constexpr int ST_BYTES = QT * kTile * 4;        // one staged tile of scores
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_OP = OFF_Q + Q_BYTES;
   static constexpr int OFF_STG = OFF_OP + S * OP_BYTES;
   static constexpr int OFF_TOPK = OFF_STG + SS * STG_BYTES;
-  static constexpr int OFF_W = OFF_TOPK + QT * CAP * 8;
-  static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;  // head weights, double-buffered
-  static constexpr int OFF_MISC = OFF_HIST + NG * 512 * 4;  // per-warp packed histograms
-  static constexpr int MISC_BYTES = 1024;
+  static constexpr int OFF_ST = OFF_TOPK + QT * CAP * 8;
+  static constexpr int OFF_W = OFF_ST + NST * ST_BYTES;
+  static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;   // head weights, double-buffered
+  static constexpr int OFF_MISC = OFF_HIST + NTK * 512 * 4;  // per-warp packed histograms
+  static constexpr int MISC_BYTES = 2048;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(CAP % 128 == 0 && CAP >= KSEL + 128, "capacity");
+  static_assert(NTHREADS <= 1024, "block size");
 };
 
 struct Misc {
   uint64_t op_full[8], op_empty[8], stg_full[8], stg_empty[8];
   uint64_t tm_full[2], tm_empty[2], q_full, q_empty, fin, w_full[2], w_empty[2];
+  uint64_t st_full[16], st_empty[16];
   uint32_t tmem_base;
   int abort;
   int cnt[4];
   unsigned long long thr[4];
-  int gok[4], glast[4], gdigit[4], gabove[4], gcd[4];
+  int gok[4], glast[4], gdigit[4], gabove[4], gcd[4];  // per top-k group
   int wsum[4][2][4];
   unsigned long long gmin[4][4], gmax[4][4];
 };
-static_assert(sizeof(Misc) <= 1024, "misc");
+static_assert(sizeof(Misc) <= 2048, "misc");
 
 struct ScoreArgs {
   const int32_t* page_table;
@@ -719,6 +728,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
   uint8_t* sStg = sm + C::OFF_STG;
   uint64_t* sTopk = reinterpret_cast<uint64_t*>(sm + C::OFF_TOPK);
   float* sW = reinterpret_cast<float*>(sm + C::OFF_W);
+  float* sSt = reinterpret_cast<float*>(sm + C::OFF_ST);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(sm + C::OFF_HIST);
   Misc* ms = reinterpret_cast<Misc*>(sm + C::OFF_MISC);
 
@@ -736,13 +746,17 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->tm_full[i], 1);
-      mbar_init(&ms->tm_empty[i], C::NEPI);
+      mbar_init(&ms->tm_empty[i], C::NSW);
+    }
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&ms->st_full[i], C::NSW);
+      mbar_init(&ms->st_empty[i], 4 * C::NTK);
     }
     mbar_init(&ms->q_full, 1);
     mbar_init(&ms->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->w_full[i], 1);
-      mbar_init(&ms->w_empty[i], C::NG);
+      mbar_init(&ms->w_empty[i], C::NSW);
     }
     mbar_init(&ms->fin, 1);
     ms->abort = 0;
@@ -929,49 +943,28 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       mbar_wait(&ms->fin, 0, 200000000LL);
     }
     __syncwarp();
-  } else if (warp < 2 + C::NEPI) {
-    // ---------------------------------------------------------- epilogue
-    const int g = (warp - 2) >> 2;
-    const int gt = threadIdx.x - 32 * (2 + 4 * g);
+  } else if (warp < C::W_TOPK) {
+    // ---------------------------------------------------------- score warps
+    // Warp w reads its 32 TMEM lanes (keys) of query j's 64 columns, frees
+    // the accumulator as soon as they are in registers, reduces them to
+    // one score per key (ReLU, head weights, fp8 key scale) and stages the
+    // scores, -inf for keys that are masked or in an invalid page.
+    const int j0 = ((warp - C::W_SCORE) >> 2) * C::QSW;  // this warp's first query
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
-    const int barid = 1 + g;
-    uint32_t* hist = sHist + g * 512;
-    int tile_seq = 0;
+    int tile_seq = 0, seg_i = 0;
     Seg s;
     bool stop = false;
-    int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
-    unsigned long long* partials =
-        reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
-    int seg_i = 0;
     while (!stop && it.next(s)) {
       const int32_t* pt = a.page_table + static_cast<long long>(s.b) * a.max_pages;
-      const float* sWs = sW + (seg_i & 1) * (QT * 64);
-      int lim[C::QPG];
-      unsigned long long thr[C::QPG];
-#pragma unroll
-      for (int jj = 0; jj < C::QPG; ++jj) {
-        const int j = g * C::QPG + jj;
-        if (gt == 0) {
-          ms->cnt[j] = 0;
-          ms->thr[j] = 0;
-        }
-        lim[jj] = j < s.nrows ? (a.causal ? s.qpos0 + j + 1 : s.L) : 0;
-        thr[jj] = 0;
-      }
-      // the producer loads this tile's head weights into buffer seg_i & 1
-      if (gt == 0) ms->gok[g] = mbar_wait(&ms->w_full[seg_i & 1], (seg_i >> 1) & 1) && !*abort_flag;
-      named_bar(barid, 128);
-      if (!ms->gok[g]) {
-        if (gt == 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ms->w_full[seg_i & 1], (seg_i >> 1) & 1))) {
+        if (lane == 0) {
           atomicOr(a.status, DSA_DEV_TIMEOUT);
           *abort_flag = 1;
         }
         break;
       }
-      static_assert(C::QPG == 1, "one query per epilogue group");
-      const int j = g;
-      const float4* w4 = reinterpret_cast<const float4*>(sWs + j * 64);
+      const float* sWs = sW + (seg_i & 1) * (QT * 64);
       for (int t = s.t0; t < s.t1; ++t) {
         const int pos = t * kTile + row;
         int pid = -1;
@@ -986,50 +979,134 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
                 a.cache + static_cast<long long>(pid) * kPageBytesFp8 + 64 * 128 + (pos & 63) * 4));
         }
         const int buf = tile_seq & 1, ub = tile_seq >> 1;
-        // every thread waits for the accumulators; a warp that gives up skips
-        // the tile, and the group agrees after the tile's barrier
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&ms->tm_full[buf], ub & 1));
-        bool pass = false;
-        uint64_t key = 0;
-        if (ok) {
-          tc_fence_after();
+        const int st = tile_seq % C::NST, us = tile_seq / C::NST;
+        if (!__all_sync(0xffffffffu, mbar_wait(&ms->tm_full[buf], ub & 1))) {
+          if (lane == 0) {
+            atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        float scs[C::QSW];
+#pragma unroll
+        for (int jj = 0; jj < C::QSW; ++jj) {
+          const int j = j0 + jj;
           const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) +
                               static_cast<uint32_t>(buf * C::N + j * 64);
-          float v[64];
-          tmem_ld64(tl, v);
-          tmem_ld_wait();
+          const float4* w4 = reinterpret_cast<const float4*>(sWs + j * 64);
+          // two halves of 32 columns through one register buffer
+          float v[32];
           unsigned long long a2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-          for (int h4 = 0; h4 < 16; ++h4) {
-            const float4 ww = w4[h4];
-            const int b = (h4 & 1) * 2;
-            a2[b + 0] = ffma2(ww.x, ww.y, fmaxf(v[4 * h4 + 0], 0.f), fmaxf(v[4 * h4 + 1], 0.f), a2[b + 0]);
-            a2[b + 1] = ffma2(ww.z, ww.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f), a2[b + 1]);
+          for (int half = 0; half < 2; ++half) {
+            tmem_ld32(tl + half * 32, v);
+            tmem_ld_wait_regs(v);
+            if (jj == C::QSW - 1 && half == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ms->tm_empty[buf]);  // accumulators are in registers
+            }
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 ww = w4[half * 8 + h4];
+              const int b = (h4 & 1) * 2;
+              a2[b + 0] = ffma2(ww.x, ww.y, fmaxf(v[4 * h4 + 0], 0.f), fmaxf(v[4 * h4 + 1], 0.f), a2[b + 0]);
+              a2[b + 1] = ffma2(ww.z, ww.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f), a2[b + 1]);
+            }
           }
           float acc[8];
 #pragma unroll
           for (int i = 0; i < 4; ++i) unpack2(a2[i], acc[2 * i], acc[2 * i + 1]);
           float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
           if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
-          key = make_key(sc, pos);
-          pass = pid >= 0 && pos < lim[0] && key > thr[0];
-        } else if (lane == 0) {
-          atomicOr(a.status, DSA_DEV_TIMEOUT);
-          *abort_flag = 1;
-          ms->gok[g] = 0;
+          const int lim = j < s.nrows ? (a.causal ? s.qpos0 + j + 1 : s.L) : 0;
+          if (pid < 0 || pos >= lim) sc = -__int_as_float(0x7f800000);
+          scs[jj] = sc;
         }
-        push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ms->tm_empty[buf]);
-        named_bar(barid, 128);
-        if (!ms->gok[g]) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&ms->st_empty[st], (us & 1) ^ 1))) {
+          if (lane == 0) {
+            atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
           stop = true;
           break;
         }
-        if (ms->cnt[j] > C::CAP - kTile)
-          group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
-        thr[0] = ms->thr[j];
+#pragma unroll
+        for (int jj = 0; jj < C::QSW; ++jj) sSt[st * (QT * kTile) + (j0 + jj) * kTile + row] = scs[jj];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->st_full[st]);
+        ++tile_seq;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ms->w_empty[seg_i & 1]);  // this warp is done with the weights
+      ++seg_i;
+    }
+  } else if (warp < C::W_CONV) {
+    // ---------------------------------------------------------- top-k groups
+    // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile: it
+    // filters the staged scores against each query's running threshold,
+    // keeps the survivors in shared memory, compacts them by radix select
+    // when the buffer fills, and at the end of the query tile selects,
+    // sorts and writes the row (or publishes a partial list and, if it is
+    // the last piece, merges them).
+    const int tg = (warp - C::W_TOPK) >> 2;
+    const int gt = threadIdx.x - 32 * (C::W_TOPK + 4 * tg);
+    const int barid = 1 + tg;
+    uint32_t* hist = sHist + tg * 512;
+    const int g = tg;
+    int tile_seq = 0;
+    Seg s;
+    bool stop = false;
+    int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
+    unsigned long long* partials =
+        reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
+    while (!stop && it.next(s)) {
+      unsigned long long thr[C::QPT];
+#pragma unroll
+      for (int jj = 0; jj < C::QPT; ++jj) {
+        const int j = tg * C::QPT + jj;
+        if (gt == 0) {
+          ms->cnt[j] = 0;
+          ms->thr[j] = 0;
+        }
+        thr[jj] = 0;
+      }
+      if (gt == 0) ms->gok[tg] = 1;
+      named_bar(barid, 128);
+      for (int t = s.t0; t < s.t1; ++t) {
+        const int pos = t * kTile + gt;
+        const int st = tile_seq % C::NST, us = tile_seq / C::NST;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&ms->st_full[st], us & 1));
+        if (ok) {
+#pragma unroll
+          for (int jj = 0; jj < C::QPT; ++jj) {
+            const int j = tg * C::QPT + jj;
+            const float sc = sSt[st * (QT * kTile) + j * kTile + gt];
+            const uint64_t key = make_key(sc, pos);
+            const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
+            push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ms->st_empty[st]);
+        } else if (lane == 0) {
+          atomicOr(a.status, DSA_DEV_TIMEOUT);
+          *abort_flag = 1;
+          ms->gok[tg] = 0;
+        }
+        named_bar(barid, 128);
+        if (!ms->gok[tg]) {
+          stop = true;
+          break;
+        }
+#pragma unroll
+        for (int jj = 0; jj < C::QPT; ++jj) {
+          const int j = tg * C::QPT + jj;
+          if (ms->cnt[j] > C::CAP - kTile)
+            group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+          thr[jj] = ms->thr[j];
+        }
         ++tile_seq;
       }
       if (stop) break;
@@ -1037,8 +1114,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       // ------------------------------------------------ finish the segment
       if (s.whole) {
 #pragma unroll
-        for (int jj = 0; jj < C::QPG; ++jj) {
-          const int j = g * C::QPG + jj;
+        for (int jj = 0; jj < C::QPT; ++jj) {
+          const int j = tg * C::QPT + jj;
           group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
           if (j < s.nrows) {
             const long long o = static_cast<long long>(s.row0 + j) * KSEL;
@@ -1052,8 +1129,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         // sorted top-k; the last piece to finish merges all of them
         const int slot = partial_slot(cta, s.qstart, total, Ge);
 #pragma unroll
-        for (int jj = 0; jj < C::QPG; ++jj) {
-          const int j = g * C::QPG + jj;
+        for (int jj = 0; jj < C::QPT; ++jj) {
+          const int j = tg * C::QPT + jj;
           group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
           if (j < s.nrows) {
             uint64_t v[KSEL / 128];
@@ -1066,15 +1143,15 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         const int cf = owner_of(s.qstart + ovh, total, Ge);  // owner of key tile 0
         const int cl = owner_of(s.qend - 1, total, Ge);
         if (gt == 0) {
-          const int old = atomicAdd(&counters[s.qt * C::NG + g], 1);
-          ms->glast[g] = (old == cl - cf);
+          const int old = atomicAdd(&counters[s.qt * C::NTK + tg], 1);
+          ms->glast[tg] = (old == cl - cf);
           __threadfence();
         }
         named_bar(barid, 128);
-        if (ms->glast[g]) {
+        if (ms->glast[tg]) {
 #pragma unroll
-          for (int jj = 0; jj < C::QPG; ++jj) {
-            const int j = g * C::QPG + jj;
+          for (int jj = 0; jj < C::QPT; ++jj) {
+            const int j = tg * C::QPT + jj;
             if (j < s.nrows) {
               uint64_t v[KSEL / 128];
               const unsigned long long* src0 =
@@ -1093,13 +1170,11 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         }
       }
       named_bar(barid, 128);
-      if (gt == 0) mbar_arrive(&ms->w_empty[seg_i & 1]);  // this group is done with the weights
-      ++seg_i;
     }
   } else {
     // ---------------------------------------------------------- fp8: e4m3 -> f16 converters
     if constexpr (FMT == DSA_FMT_FP8) {
-      const int ct = threadIdx.x - 32 * (2 + C::NEPI);
+      const int ct = threadIdx.x - 32 * C::W_CONV;
       int tile_seq = 0;
       Seg s;
       bool stop = false;
