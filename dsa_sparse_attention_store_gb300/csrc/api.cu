@@ -198,6 +198,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
   if (k != 512 && k != 1024) return DSA_ERR_UNSUPPORTED;
   if (Tq < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(num_pages) * 64 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
+  if (B > dsa::max_sequences()) return DSA_ERR_UNSUPPORTED;
   if (Tq == 0) return DSA_OK;
   if (!q || !head_w || !cache || !page_table || !seq_lens || !cu_q || !out_idx || !out_score ||
       !workspace)

@@ -88,6 +88,7 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
                         void* cache, int32_t num_pages, dsa_fmt fmt, cudaStream_t stream);
 
 size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt);
+int max_sequences();  // largest B dsa_index_topk accepts
 
 dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
                        int32_t num_pages, dsa_fmt fmt, const int32_t* page_table,

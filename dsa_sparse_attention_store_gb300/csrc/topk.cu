@@ -63,7 +63,7 @@ struct PlanHdr {
 // Per query tile: {b, row0, nrows, ntile} and {L, qpos0, 0, 0} where qpos0 is
 // the position of the tile's first query.
 struct WsLayout {
-  size_t hdr, seq_qoff, meta, prefix, counters, rec, partials, qh, wq, total;
+  size_t hdr, meta, prefix, counters, rec, partials, qh, wq, total;
   int QT, G, qtmax, NG;
 };
 
@@ -80,8 +80,6 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
   size_t o = 0;
   L.hdr = o;
   o += 256;
-  L.seq_qoff = o;
-  o = up256(o + static_cast<size_t>(B + 1) * 4);
   L.meta = o;
   o = up256(o + static_cast<size_t>(L.qtmax) * 32);
   L.prefix = o;
@@ -153,6 +151,11 @@ __device__ __forceinline__ long long range_start(int c, long long total, int G) 
 }
 
 // ------------------------------------------------------------------ plan
+// One CTA. Per-sequence sizes and query-tile offsets live in shared memory
+// (B <= kMaxSeqs), so the only global round trips are the input loads and
+// the final writes.
+constexpr int kMaxSeqs = 16384;
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ cu_q, int B, int Tq,
                                                     int QT, int NG, int causal, int max_pages, int k,
@@ -160,21 +163,30 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     float* out_score, unsigned int* status) {
   __shared__ int smi[32];
   __shared__ long long sml[32];
+  extern __shared__ int plan_sm[];
+  int* s_cq = plan_sm;           // [B + 1]
+  int* s_len = s_cq + (B + 1);   // [B]
+  int* s_qoff = s_len + B;       // [B + 1]
   pdl_wait();
   pdl_trigger();
   PlanHdr* hdr = reinterpret_cast<PlanHdr*>(ws + L.hdr);
-  int* qoff = reinterpret_cast<int*>(ws + L.seq_qoff);
   int4* meta = reinterpret_cast<int4*>(ws + L.meta);
   long long* prefix = reinterpret_cast<long long*>(ws + L.prefix);
   int* cnt = reinterpret_cast<int*>(ws + L.counters);
   int* rec = reinterpret_cast<int*>(ws + L.rec);
+
+  for (int i = threadIdx.x; i <= B; i += 1024) {
+    s_cq[i] = cu_q[i];
+    if (i < B) s_len[i] = seq_lens[i];
+  }
+  __syncthreads();
 
   int carry = 0;
   for (int base = 0; base < B; base += 1024) {
     const int b = base + threadIdx.x;
     int v = 0;
     if (b < B) {
-      const int q0 = cu_q[b], q1 = cu_q[b + 1], Ls = seq_lens[b];
+      const int q0 = s_cq[b], q1 = s_cq[b + 1], Ls = s_len[b];
       const int nq = q1 - q0;
       const bool ok = q0 >= 0 && nq >= 0 && q1 <= Tq && Ls >= nq &&
                       static_cast<long long>(Ls) <= static_cast<long long>(max_pages) * 64;
@@ -183,10 +195,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
     int tot;
     const int ex = block_excl_scan<int>(v, smi, tot);
-    if (b < B) qoff[b] = carry + ex;
+    if (b < B) s_qoff[b] = carry + ex;
     carry += tot;
   }
-  if (threadIdx.x == 0) qoff[B] = carry;
+  if (threadIdx.x == 0) s_qoff[B] = carry;
   __syncthreads();
   const int qtot = carry;
 
@@ -199,11 +211,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       int lo = 0, hi = B - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (qoff[mid] <= qt) lo = mid; else hi = mid - 1;
+        if (s_qoff[mid] <= qt) lo = mid; else hi = mid - 1;
       }
       const int b = lo;
-      const int t = qt - qoff[b];
-      const int q0 = cu_q[b], nq = cu_q[b + 1] - q0, Ls = seq_lens[b];
+      const int t = qt - s_qoff[b];
+      const int q0 = s_cq[b], nq = s_cq[b + 1] - q0, Ls = s_len[b];
       const int row0 = q0 + t * QT;
       const int nrows = min(QT, nq - t * QT);
       const int qpos0 = Ls - nq + t * QT;
@@ -246,9 +258,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     int c = static_cast<int>(p0 * Ge / total);
     while (c > 0 && range_start(c, total, Ge) >= p0) --c;
     for (; c < Ge; ++c) {
-      const long long s = range_start(c, total, Ge);
-      if (s >= p1) break;
-      if (s >= p0) rec[c] = qt;
+      const long long st = range_start(c, total, Ge);
+      if (st >= p1) break;
+      if (st >= p0) rec[c] = qt;
     }
   }
 }
@@ -1263,6 +1275,8 @@ dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtenso
 
 }  // namespace
 
+int max_sequences() { return kMaxSeqs; }
+
 size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt) {
   return ws_layout(ctx->num_sms, Tq, B, k, fmt).total;
 }
@@ -1278,7 +1292,11 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
     const int ovh = L.QT == 4 ? 12 : 4;  // measured fixed cost of a query tile, in key tiles
-    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, seq_lens, cu_q, B, Tq, L.QT, L.NG,
+    const size_t psm = static_cast<size_t>(3 * B + 2) * sizeof(int);
+    if (cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(psm)) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    if (launch_pdl(plan_kernel, dim3(1), dim3(1024), psm, stream, seq_lens, cu_q, B, Tq, L.QT, L.NG,
                    causal, max_pages, k, ovh, ws, L, out_idx, out_score, ctx->status) != cudaSuccess)
       return DSA_ERR_CUDA;
   }

@@ -132,7 +132,7 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  *              page are not read.
  *  seq_lens    (device) [B] int32, n_q(b) <= seq_lens[b] <= 64*max_pages.
  *  cu_q        (device) [B+1] int32, cu_q[0] = 0, non-decreasing, cu_q[B] = Tq.
- *  k           512 or 1024.
+ *  k           512 or 1024.  B <= 16384 (else DSA_ERR_UNSUPPORTED).
  *  out_idx     (device) [Tq][k] int32;  out_score (device) [Tq][k] fp32.
  *  workspace   (device) >= dsa_index_topk_workspace_size(...) bytes, 256-byte
  *              aligned; contents need not be initialised and are scratch.
