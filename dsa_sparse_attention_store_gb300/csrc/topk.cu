@@ -977,19 +977,34 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         break;
       }
       const float* sWs = sW + (seg_i & 1) * (QT * 64);
+      // page id of this thread's key in tile tt (-1: past the sequence or
+      // out of range), and the fp8 key's scale; issued ahead of use so the
+      // global-memory latency overlaps earlier tiles (page ids two tiles
+      // ahead, scales one tile ahead)
+      auto page_of = [&](int tt) -> int {
+        const int p = tt * kTile + row;
+        if (tt >= s.t1 || p >= s.L) return -1;
+        const int v = pt[p >> 6];
+        return (v < 0 || v >= a.num_pages) ? -1 : v;
+      };
+      auto scale_of = [&](int id, int tt) -> float {
+        if constexpr (FMT == DSA_FMT_FP8) {
+          if (id >= 0)
+            return __ldg(reinterpret_cast<const float*>(a.cache + static_cast<long long>(id) * kPageBytesFp8 +
+                                                        64 * 128 + ((tt * kTile + row) & 63) * 4));
+        }
+        return 1.f;
+      };
+      int pid_n1 = page_of(s.t0);
+      int pid_n2 = page_of(s.t0 + 1);
+      float scale_n1 = scale_of(pid_n1, s.t0);
       for (int t = s.t0; t < s.t1; ++t) {
         const int pos = t * kTile + row;
-        int pid = -1;
-        if (pos < s.L) {
-          pid = pt[pos >> 6];
-          if (pid < 0 || pid >= a.num_pages) pid = -1;
-        }
-        float kscale = 1.f;
-        if constexpr (FMT == DSA_FMT_FP8) {
-          if (pid >= 0)
-            kscale = __ldg(reinterpret_cast<const float*>(
-                a.cache + static_cast<long long>(pid) * kPageBytesFp8 + 64 * 128 + (pos & 63) * 4));
-        }
+        const int pid = pid_n1;
+        const float kscale = scale_n1;
+        pid_n1 = pid_n2;
+        pid_n2 = page_of(t + 2);
+        scale_n1 = scale_of(pid_n1, t + 1);
         const int buf = tile_seq & 1, ub = tile_seq >> 1;
         const int st = tile_seq % C::NST, us = tile_seq / C::NST;
         if (!__all_sync(0xffffffffu, mbar_wait(&ms->tm_full[buf], ub & 1))) {
