@@ -27,11 +27,17 @@
 //             warp 0      producer: page-table lookups, TMA of 64-token pages
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
 //                         x K=128 into one of two TMEM accumulators
-//             4*NG warps  epilogue: tcgen05.ld, ReLU, head-weighted sum, mask,
-//                         threshold filter into the running top-k; at the end
-//                         of a query tile: exact selection, sort, output
-//             4 warps     (fp8) e4m3 -> f16 conversion of staged key tiles
-//           Keys sit on the MMA's M dimension so each epilogue thread owns one
+//             score warps tcgen05.ld, ReLU, head-weighted sum, fp8 key
+//                         scale, mask; one score per key staged in a ring of
+//                         shared-memory slots
+//             top-k groups of 4 warps: threshold filter of the staged scores
+//                         into a running top-k per query, compacted by radix
+//                         select when full; at the end of a query tile exact
+//                         selection, sort and output (or, for a query tile
+//                         split across CTAs, a sorted partial list, merged by
+//                         the piece that finishes last)
+//             fp8 only    e4m3 -> f16 conversion of staged key tiles
+//           Keys sit on the MMA's M dimension so each score thread owns one
 //           key (one TMEM lane) and reduces over heads in its own registers.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -307,12 +313,21 @@ struct Cfg {
   static constexpr int N = 64 * QT;                      // MMA N: queries x heads
   static constexpr int QSW = QT == 4 ? 2 : 1;            // queries per score warp
   static constexpr int NSW = 4 * QT / QSW;               // score warps (4 cover the 128 lanes)
-  static constexpr int NTK = QT;                         // top-k groups of 4 warps, one per query
-  static constexpr int QPT = QT / NTK;                   // queries per top-k group
-  static constexpr int NG = NTK;
+  // top-k groups of 4 warps: one per query, except for one-query tiles,
+  // where two groups take alternate query tiles so that one group's final
+  // selection overlaps the other's filtering of the next tile's keys
+  static constexpr bool ALT = QT == 1;
+  static constexpr int NTK = ALT ? 2 : QT;
+  static constexpr int QPT = ALT ? 1 : QT / NTK;         // queries per top-k group
+  static constexpr int NBUF = ALT ? 2 : QT;              // running top-k buffers
   static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 2) : (FMT == DSA_FMT_BF16 ? 5 : 2);
   static constexpr int SS = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // e4m3 staging
   static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
+  // alternating groups each read their own ring of staging slots: a group
+  // that skips the other's query tile must not wait on a slot phase that
+  // the score warps have not reached yet
+  static constexpr int NRING = ALT ? 2 : 1;
+  static constexpr int RS = NST / NRING;                 // slots per ring
   // running top-k capacity per query
   static constexpr int CAP = QT == 4 ? 1280 : (KSEL == 512 ? 1280 : 2048);
   static constexpr int NCONV = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // converter warps
@@ -330,7 +345,7 @@ struct Cfg {
   static constexpr int OFF_OP = OFF_Q + Q_BYTES;
   static constexpr int OFF_STG = OFF_OP + S * OP_BYTES;
   static constexpr int OFF_TOPK = OFF_STG + SS * STG_BYTES;
-  static constexpr int OFF_ST = OFF_TOPK + QT * CAP * 8;
+  static constexpr int OFF_ST = OFF_TOPK + NBUF * CAP * 8;
   static constexpr int OFF_W = OFF_ST + NST * ST_BYTES;
   static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;   // head weights, double-buffered
   static constexpr int OFF_MISC = OFF_HIST + NTK * 512 * 4;  // per-warp packed histograms
@@ -607,6 +622,24 @@ __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, 
   named_bar(barid, 128);
 }
 
+// Compare-exchange of registers e and e ^ JE of each lane (stride 32 * JE).
+template <int K, int JE>
+__device__ __forceinline__ void bitonic_reg_stage(uint64_t (&v)[K / 128], int size, int w, int lane) {
+  constexpr int PW = K / 4;
+  constexpr int E = PW / 32;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if ((e ^ JE) > e) {
+      const int x = w * PW + e * 32 + lane;
+      const bool desc = (x & size) == 0;
+      const uint64_t a = v[e], b = v[e ^ JE];
+      const bool sw = desc ? (a < b) : (a > b);
+      v[e] = sw ? b : a;
+      v[e ^ JE] = sw ? a : b;
+    }
+  }
+}
+
 // Bitonic sorting network over K slots held by one group of 128 threads:
 // warp w owns slots [w*K/4, (w+1)*K/4); slot x = w*K/4 + e*32 + lane is
 // v[e] of that lane. Strides below 32 use shuffles, strides inside a warp's
@@ -634,19 +667,10 @@ __device__ __forceinline__ void bitonic_stage(uint64_t (&v)[K / 128], int size, 
       v[e] = (lower == desc) ? mx : mn;
     }
   } else if (stride >= 32) {
-    const int je = stride >> 5;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int e2 = e ^ je;
-      if (e2 > e) {
-        const int x = w * PW + e * 32 + lane;
-        const bool desc = (x & size) == 0;
-        const uint64_t a = v[e], b = v[e2];
-        const bool sw = desc ? (a < b) : (a > b);
-        v[e] = sw ? b : a;
-        v[e2] = sw ? a : b;
-      }
-    }
+    // register index must be a compile-time constant: one branch per stride
+    if constexpr (E >= 2) if (stride == 32) bitonic_reg_stage<K, 1>(v, size, w, lane);
+    if constexpr (E >= 4) if (stride == 64) bitonic_reg_stage<K, 2>(v, size, w, lane);
+    if constexpr (E >= 8) if (stride == 128) bitonic_reg_stage<K, 4>(v, size, w, lane);
   } else {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -662,8 +686,11 @@ __device__ __forceinline__ void bitonic_stage(uint64_t (&v)[K / 128], int size, 
 }
 
 // Sort buf[0..n) (n <= K, distinct keys) descending into registers; slots
-// past n hold 0 (below every key).
-template <int K>
+// past n hold 0 (below every key). ROLL keeps the network as loops: fully
+// unrolled it is tens of KB of code, which pays where a CTA sorts many rows
+// (the code stays cached) but not where it sorts once or twice (fetching the
+// code cold costs more than the loop control).
+template <int K, bool ROLL>
 __device__ void group_sort_regs(uint64_t* buf, int n, uint64_t (&v)[K / 128], int gt, int barid) {
   constexpr int PW = K / 4;
   constexpr int E = PW / 32;
@@ -673,10 +700,18 @@ __device__ void group_sort_regs(uint64_t* buf, int n, uint64_t (&v)[K / 128], in
     const int x = w * PW + e * 32 + lane;
     v[e] = x < n ? buf[x] : 0ull;
   }
+  if constexpr (ROLL) {
+#pragma unroll 1
+    for (int size = 2; size <= K; size <<= 1) {
+#pragma unroll 1
+      for (int stride = size >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, size, stride, buf, w, lane, barid);
+    }
+  } else {
 #pragma unroll
-  for (int size = 2; size <= K; size <<= 1) {
+    for (int size = 2; size <= K; size <<= 1) {
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, size, stride, buf, w, lane, barid);
+      for (int stride = size >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, size, stride, buf, w, lane, barid);
+    }
   }
   named_bar(barid, 128);
 }
@@ -685,7 +720,7 @@ __device__ void group_sort_regs(uint64_t* buf, int n, uint64_t (&v)[K / 128], in
 // src (K keys, global memory), sorted descending: the elementwise max of v and
 // src reversed is a bitonic sequence holding the K largest, and one bitonic
 // merge sorts it.
-template <int K>
+template <int K, bool ROLL>
 __device__ void group_merge_regs(uint64_t (&v)[K / 128], const unsigned long long* src,
                                  uint64_t* xbuf, int gt, int barid) {
   constexpr int PW = K / 4;
@@ -698,7 +733,13 @@ __device__ void group_merge_regs(uint64_t (&v)[K / 128], const unsigned long lon
     v[e] = v[e] > o ? v[e] : o;
   }
 #pragma unroll
-  for (int stride = K >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
+  if constexpr (ROLL) {
+#pragma unroll 1
+    for (int stride = K >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
+  } else {
+#pragma unroll
+    for (int stride = K >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
+  }
   named_bar(barid, 128);
 }
 
@@ -762,7 +803,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     }
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ms->st_full[i], C::NSW);
-      mbar_init(&ms->st_empty[i], 4 * C::NTK);
+      mbar_init(&ms->st_empty[i], C::ALT ? 4 : 4 * C::NTK);
     }
     mbar_init(&ms->q_full, 1);
     mbar_init(&ms->q_empty, 1);
@@ -964,7 +1005,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     const int j0 = ((warp - C::W_SCORE) >> 2) * C::QSW;  // this warp's first query
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
-    int tile_seq = 0, seg_i = 0;
+    int tile_seq = 0, seg_i = 0, rq0 = 0, rq1 = 0;
     Seg s;
     bool stop = false;
     while (!stop && it.next(s)) {
@@ -977,6 +1018,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         break;
       }
       const float* sWs = sW + (seg_i & 1) * (QT * 64);
+      const int ring = C::ALT ? (seg_i & 1) : 0;
+      int rq = ring ? rq1 : rq0;  // tiles staged so far in this ring
       // page id of this thread's key in tile tt (-1: past the sequence or
       // out of range), and the fp8 key's scale; issued ahead of use so the
       // global-memory latency overlaps earlier tiles (page ids two tiles
@@ -1006,7 +1049,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         pid_n2 = page_of(t + 2);
         scale_n1 = scale_of(pid_n1, t + 1);
         const int buf = tile_seq & 1, ub = tile_seq >> 1;
-        const int st = tile_seq % C::NST, us = tile_seq / C::NST;
+        const int sq = C::ALT ? rq : tile_seq;
+        const int st = ring * C::RS + sq % C::RS, us = sq / C::RS;
         if (!__all_sync(0xffffffffu, mbar_wait(&ms->tm_full[buf], ub & 1))) {
           if (lane == 0) {
             atomicOr(a.status, DSA_DEV_TIMEOUT);
@@ -1065,6 +1109,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ms->st_full[st]);
         ++tile_seq;
+        ++rq;
+      }
+      if constexpr (C::ALT) {
+        if (ring) rq1 = rq; else rq0 = rq;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ms->w_empty[seg_i & 1]);  // this warp is done with the weights
@@ -1072,7 +1120,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     }
   } else if (warp < C::W_CONV) {
     // ---------------------------------------------------------- top-k groups
-    // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile: it
+    // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile (of
+    // every other query tile, query 0, when the tiles hold one query): it
     // filters the staged scores against each query's running threshold,
     // keeps the survivors in shared memory, compacts them by radix select
     // when the buffer fills, and at the end of the query tile selects,
@@ -1083,20 +1132,24 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     const int barid = 1 + tg;
     uint32_t* hist = sHist + tg * 512;
     const int g = tg;
-    int tile_seq = 0;
+    int tile_seq = 0, seg_i = 0;
     Seg s;
     bool stop = false;
     int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
     unsigned long long* partials =
         reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
+    // query jj of this group in the tile, and its running top-k buffer
+    auto qrow = [&](int jj) { return C::ALT ? jj : tg * C::QPT + jj; };
+    auto qbuf = [&](int jj) { return C::ALT ? tg : tg * C::QPT + jj; };
     while (!stop && it.next(s)) {
+      if (C::ALT && (seg_i++ & 1) != tg) continue;  // the other group's query tile
       unsigned long long thr[C::QPT];
 #pragma unroll
       for (int jj = 0; jj < C::QPT; ++jj) {
-        const int j = tg * C::QPT + jj;
+        const int jb = qbuf(jj);
         if (gt == 0) {
-          ms->cnt[j] = 0;
-          ms->thr[j] = 0;
+          ms->cnt[jb] = 0;
+          ms->thr[jb] = 0;
         }
         thr[jj] = 0;
       }
@@ -1104,16 +1157,17 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       named_bar(barid, 128);
       for (int t = s.t0; t < s.t1; ++t) {
         const int pos = t * kTile + gt;
-        const int st = tile_seq % C::NST, us = tile_seq / C::NST;
+        // this group's ring (the only ring unless the groups alternate)
+        const int st = (C::ALT ? tg : 0) * C::RS + tile_seq % C::RS, us = tile_seq / C::RS;
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&ms->st_full[st], us & 1));
         if (ok) {
 #pragma unroll
           for (int jj = 0; jj < C::QPT; ++jj) {
-            const int j = tg * C::QPT + jj;
+            const int j = qrow(jj), jb = qbuf(jj);
             const float sc = sSt[st * (QT * kTile) + j * kTile + gt];
             const uint64_t key = make_key(sc, pos);
             const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
-            push_key(pass, key, sTopk + j * C::CAP, &ms->cnt[j], lane);
+            push_key(pass, key, sTopk + jb * C::CAP, &ms->cnt[jb], lane);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->st_empty[st]);
@@ -1129,10 +1183,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         }
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
-          const int j = tg * C::QPT + jj;
-          if (ms->cnt[j] > C::CAP - kTile)
-            group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
-          thr[jj] = ms->thr[j];
+          const int jb = qbuf(jj);
+          if (ms->cnt[jb] > C::CAP - kTile)
+            group_compact(sTopk + jb * C::CAP, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, g, gt, barid);
+          thr[jj] = ms->thr[jb];
         }
         ++tile_seq;
       }
@@ -1142,12 +1196,12 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       if (s.whole) {
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
-          const int j = tg * C::QPT + jj;
-          group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+          const int j = qrow(jj), jb = qbuf(jj);
+          group_compact(sTopk + jb * C::CAP, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, g, gt, barid);
           if (j < s.nrows) {
             const long long o = static_cast<long long>(s.row0 + j) * KSEL;
             uint64_t v[KSEL / 128];
-            group_sort_regs<KSEL>(sTopk + j * C::CAP, min(ms->cnt[j], KSEL), v, gt, barid);
+            group_sort_regs<KSEL, QT == 1>(sTopk + jb * C::CAP, min(ms->cnt[jb], KSEL), v, gt, barid);
             write_row<KSEL>(v, a.out_idx + o, a.out_score + o, gt);
           }
         }
@@ -1157,11 +1211,11 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         const int slot = partial_slot(cta, s.qstart, total, Ge);
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
-          const int j = tg * C::QPT + jj;
-          group_compact(sTopk + j * C::CAP, &ms->cnt[j], &ms->thr[j], KSEL, hist, ms, g, gt, barid);
+          const int j = qrow(jj), jb = qbuf(jj);
+          group_compact(sTopk + jb * C::CAP, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, g, gt, barid);
           if (j < s.nrows) {
             uint64_t v[KSEL / 128];
-            group_sort_regs<KSEL>(sTopk + j * C::CAP, min(ms->cnt[j], KSEL), v, gt, barid);
+            group_sort_regs<KSEL, QT == 1>(sTopk + jb * C::CAP, min(ms->cnt[jb], KSEL), v, gt, barid);
             write_keys<KSEL>(v, partials + (static_cast<long long>(slot) * QT + j) * KSEL, gt);
           }
         }
@@ -1170,7 +1224,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         const int cf = owner_of(s.qstart + ovh, total, Ge);  // owner of key tile 0
         const int cl = owner_of(s.qend - 1, total, Ge);
         if (gt == 0) {
-          const int old = atomicAdd(&counters[s.qt * C::NTK + tg], 1);
+          // one counter per query tile and group (per query tile when the
+          // groups alternate: its pieces may sit in either group)
+          const int old = atomicAdd(&counters[s.qt * QT + (C::ALT ? 0 : tg)], 1);
           ms->glast[tg] = (old == cl - cf);
           __threadfence();
         }
@@ -1178,7 +1234,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         if (ms->glast[tg]) {
 #pragma unroll
           for (int jj = 0; jj < C::QPT; ++jj) {
-            const int j = tg * C::QPT + jj;
+            const int j = qrow(jj), jb = qbuf(jj);
             if (j < s.nrows) {
               uint64_t v[KSEL / 128];
               const unsigned long long* src0 =
@@ -1188,7 +1244,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
               for (int c = cf + 1; c <= cl; ++c) {
                 const unsigned long long* src =
                     partials + (static_cast<long long>(partial_slot(c, s.qstart, total, Ge)) * QT + j) * KSEL;
-                group_merge_regs<KSEL>(v, src, sTopk + j * C::CAP, gt, barid);
+                group_merge_regs<KSEL, QT == 1>(v, src, sTopk + jb * C::CAP, gt, barid);
               }
               const long long o = static_cast<long long>(s.row0 + j) * KSEL;
               write_row<KSEL>(v, a.out_idx + o, a.out_score + o, gt);
