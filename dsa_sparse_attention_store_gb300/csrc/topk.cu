@@ -328,8 +328,9 @@ struct Cfg {
   // the score warps have not reached yet
   static constexpr int NRING = ALT ? 2 : 1;
   static constexpr int RS = NST / NRING;                 // slots per ring
-  // running top-k capacity per query
-  static constexpr int CAP = QT == 4 ? 1280 : (KSEL == 512 ? 1280 : 2048);
+  // keys of one query's running top-k: sorted list + batch of KSEL each
+  // (one-query tiles), else a candidate buffer cut back by radix select
+  static constexpr int TK = ALT ? 2 * KSEL : 1280;
   static constexpr int NCONV = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // converter warps
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
@@ -345,14 +346,14 @@ struct Cfg {
   static constexpr int OFF_OP = OFF_Q + Q_BYTES;
   static constexpr int OFF_STG = OFF_OP + S * OP_BYTES;
   static constexpr int OFF_TOPK = OFF_STG + SS * STG_BYTES;
-  static constexpr int OFF_ST = OFF_TOPK + NBUF * CAP * 8;
+  static constexpr int OFF_ST = OFF_TOPK + NBUF * TK * 8;
   static constexpr int OFF_W = OFF_ST + NST * ST_BYTES;
   static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;   // head weights, double-buffered
-  static constexpr int OFF_MISC = OFF_HIST + NTK * 512 * 4;  // per-warp packed histograms
+  static constexpr int OFF_MISC = OFF_HIST + (ALT ? 0 : NTK * 512 * 4);  // radix-select histograms
   static constexpr int MISC_BYTES = 2048;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(CAP % 128 == 0 && CAP >= KSEL + 128, "capacity");
+  static_assert(ALT || (TK % 128 == 0 && TK >= KSEL + 128), "candidate buffer");
   static_assert(NTHREADS <= 1024, "block size");
 };
 
@@ -458,6 +459,24 @@ __device__ __forceinline__ int partial_slot(int c, long long qt_start, long long
 }
 
 // ------------------------------------------------------------------ running top-k (one group of 128 threads)
+// Keys above a query's threshold are appended to a shared-memory buffer as
+// tiles arrive. Two ways to keep the buffer bounded:
+//   * list + batch (one-query tiles): the running top-k is a list L of K keys
+//     sorted in descending order (key 0 marks an empty slot); a nearly full
+//     batch of candidates is sorted and merged into L with bitonic networks
+//     and L's K-th key becomes the threshold. The end of a query tile then
+//     costs one partial batch, which matters when a CTA finishes few tiles.
+//   * radix select (several queries per tile): a full buffer is cut back to
+//     its K largest keys; the rare large compactions are cheaper than many
+//     batch merges when four groups share the SM with busy score warps, and
+//     the keys are sorted once at the end.
+//
+// The networks run in registers over K slots held by the group's 4 warps:
+// slot x = w*PW + lane*E + e is register e of lane `lane` of warp w
+// (PW = K/4, E = K/128). Strides below E stay inside a thread, strides up
+// to PW use shuffles, larger ones (between warps) go through a K-key
+// shared-memory exchange buffer.
+
 __device__ __forceinline__ void push_key(bool pass, uint64_t key, uint64_t* buf, int* cnt, int lane) {
   const unsigned m = __ballot_sync(0xffffffffu, pass);
   if (m) {
@@ -622,150 +641,171 @@ __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, 
   named_bar(barid, 128);
 }
 
-// Compare-exchange of registers e and e ^ JE of each lane (stride 32 * JE).
-template <int K, int JE>
-__device__ __forceinline__ void bitonic_reg_stage(uint64_t (&v)[K / 128], int size, int w, int lane) {
-  constexpr int PW = K / 4;
-  constexpr int E = PW / 32;
+// Compare-exchange of registers e and e ^ S (stride S < E) of each thread;
+// descending where (x & size) == 0.
+template <int K, int S>
+__device__ __forceinline__ void net_reg_stage(uint64_t (&v)[K / 128], int size, int w, int lane) {
+  constexpr int PW = K / 4, E = PW / 32;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    if ((e ^ JE) > e) {
-      const int x = w * PW + e * 32 + lane;
+    if ((e ^ S) > e) {
+      const int x = w * PW + lane * E + e;
       const bool desc = (x & size) == 0;
-      const uint64_t a = v[e], b = v[e ^ JE];
-      const bool sw = desc ? (a < b) : (a > b);
+      const uint64_t a = v[e], b = v[e ^ S];
+      const bool sw = (a < b) == desc;
       v[e] = sw ? b : a;
-      v[e ^ JE] = sw ? a : b;
+      v[e ^ S] = sw ? a : b;
     }
   }
 }
 
-// Bitonic sorting network over K slots held by one group of 128 threads:
-// warp w owns slots [w*K/4, (w+1)*K/4); slot x = w*K/4 + e*32 + lane is
-// v[e] of that lane. Strides below 32 use shuffles, strides inside a warp's
-// quarter compare two registers of one lane, strides that cross warps go
-// through the shared-memory array xbuf (K slots). Descending where
-// (x & size) == 0.
+// One stage of a bitonic network: slot x is compared with slot x ^ stride,
+// the lower slot keeps the larger key where (x & size) == 0 (descending
+// run) and the smaller one elsewhere.
 template <int K>
-__device__ __forceinline__ void bitonic_stage(uint64_t (&v)[K / 128], int size, int stride,
-                                              uint64_t* xbuf, int w, int lane, int barid) {
-  constexpr int PW = K / 4;
-  constexpr int E = PW / 32;
+__device__ __forceinline__ void net_stage(uint64_t (&v)[K / 128], int size, int stride, uint64_t* xbuf,
+                                          int w, int lane, int barid) {
+  constexpr int PW = K / 4, E = PW / 32;
   if (stride >= PW) {
+    const bool lower = ((w * PW) & stride) == 0;
+    const bool desc = ((w * PW) & size) == 0;
+    const bool tmax = lower == desc;
+    const int x0 = w * PW + lane * E;
     named_bar(barid, 128);
 #pragma unroll
-    for (int e = 0; e < E; ++e) xbuf[w * PW + e * 32 + lane] = v[e];
+    for (int e = 0; e < E; ++e) xbuf[x0 + e] = v[e];
     named_bar(barid, 128);
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      const int x = w * PW + e * 32 + lane;
-      const uint64_t o = xbuf[x ^ stride];
-      const bool lower = (x & stride) == 0;
-      const bool desc = (x & size) == 0;
-      const uint64_t mx = v[e] > o ? v[e] : o;
-      const uint64_t mn = v[e] > o ? o : v[e];
-      v[e] = (lower == desc) ? mx : mn;
+      const uint64_t o = xbuf[(x0 + e) ^ stride];
+      v[e] = ((v[e] > o) == tmax) ? v[e] : o;
     }
-  } else if (stride >= 32) {
-    // register index must be a compile-time constant: one branch per stride
-    if constexpr (E >= 2) if (stride == 32) bitonic_reg_stage<K, 1>(v, size, w, lane);
-    if constexpr (E >= 4) if (stride == 64) bitonic_reg_stage<K, 2>(v, size, w, lane);
-    if constexpr (E >= 8) if (stride == 128) bitonic_reg_stage<K, 4>(v, size, w, lane);
+  } else if (stride >= E) {
+    const int ls = stride / E;
+    const bool lower = (lane & ls) == 0;
+    const bool desc = ((w * PW + lane * E) & size) == 0;
+    const bool tmax = lower == desc;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], ls);
+      v[e] = ((v[e] > o) == tmax) ? v[e] : o;
+    }
   } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int x = w * PW + e * 32 + lane;
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, v[e], stride);
-      const bool lower = (lane & stride) == 0;
-      const bool desc = (x & size) == 0;
-      const uint64_t mx = v[e] > o ? v[e] : o;
-      const uint64_t mn = v[e] > o ? o : v[e];
-      v[e] = (lower == desc) ? mx : mn;
-    }
+    // register index must be a compile-time constant: one branch per stride
+    if constexpr (E > 1) if (stride == 1) net_reg_stage<K, 1>(v, size, w, lane);
+    if constexpr (E > 2) if (stride == 2) net_reg_stage<K, 2>(v, size, w, lane);
+    if constexpr (E > 4) if (stride == 4) net_reg_stage<K, 4>(v, size, w, lane);
   }
 }
 
-// Sort buf[0..n) (n <= K, distinct keys) descending into registers; slots
-// past n hold 0 (below every key). ROLL keeps the network as loops: fully
-// unrolled it is tens of KB of code, which pays where a CTA sorts many rows
-// (the code stays cached) but not where it sorts once or twice (fetching the
-// code cold costs more than the loop control).
-template <int K, bool ROLL>
-__device__ void group_sort_regs(uint64_t* buf, int n, uint64_t (&v)[K / 128], int gt, int barid) {
-  constexpr int PW = K / 4;
-  constexpr int E = PW / 32;
+// Sort the K slots descending.
+template <int K>
+__device__ __forceinline__ void net_sort(uint64_t (&v)[K / 128], uint64_t* xbuf, int w, int lane, int barid) {
+#pragma unroll
+  for (int size = 2; size <= K; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) net_stage<K>(v, size, stride, xbuf, w, lane, barid);
+  }
+}
+
+// Sort a bitonic sequence of K slots descending.
+template <int K>
+__device__ __forceinline__ void net_merge(uint64_t (&v)[K / 128], uint64_t* xbuf, int w, int lane, int barid) {
+#pragma unroll
+  for (int stride = K >> 1; stride > 0; stride >>= 1) net_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
+}
+
+// L := the K largest of L and batch[0..*cnt) (*cnt <= K); *thr := L's
+// K-th key (0 while L has empty slots); *cnt := 0. The batch buffer (K
+// keys) is the exchange buffer of the networks. The larger half of the
+// union is the elementwise maximum of the sorted batch and L reversed, a
+// bitonic sequence, so one merge network sorts it. Kept out of line: one
+// copy of the networks' code serves every call site.
+template <int K>
+__device__ __noinline__ void batch_merge(uint64_t* batch, int* cnt, uint64_t* L, unsigned long long* thr,
+                                         int gt, int barid) {
+  constexpr int PW = K / 4, E = PW / 32;
   const int w = gt >> 5, lane = gt & 31;
+  const int n = *cnt;
+  uint64_t v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {  // the batch is unordered: any slot assignment
+    const int x = w * PW + e * 32 + lane;
+    v[e] = x < n ? batch[x] : 0ull;
+  }
+  net_sort<K>(v, batch, w, lane, barid);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const uint64_t o = L[K - 1 - (w * PW + lane * E + e)];
+    v[e] = v[e] > o ? v[e] : o;
+  }
+  net_merge<K>(v, batch, w, lane, barid);
+  named_bar(barid, 128);  // every read of L is done
+#pragma unroll
+  for (int e = 0; e < E; ++e) L[w * PW + lane * E + e] = v[e];
+  if (gt == 127) *thr = v[E - 1];
+  if (gt == 0) *cnt = 0;
+  named_bar(barid, 128);
+}
+
+// Sort buf[0..n) (n <= K, distinct keys) into buf[0..K) descending, 0 in
+// the slots past n. buf (at least K keys) is the exchange buffer.
+template <int K>
+__device__ __forceinline__ void sort_list(uint64_t* buf, int n, int gt, int barid) {
+  constexpr int PW = K / 4, E = PW / 32;
+  const int w = gt >> 5, lane = gt & 31;
+  uint64_t v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int x = w * PW + e * 32 + lane;
     v[e] = x < n ? buf[x] : 0ull;
   }
-  if constexpr (ROLL) {
-#pragma unroll 1
-    for (int size = 2; size <= K; size <<= 1) {
-#pragma unroll 1
-      for (int stride = size >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, size, stride, buf, w, lane, barid);
-    }
-  } else {
+  net_sort<K>(v, buf, w, lane, barid);
+  named_bar(barid, 128);  // every read of buf is done
 #pragma unroll
-    for (int size = 2; size <= K; size <<= 1) {
-#pragma unroll
-      for (int stride = size >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, size, stride, buf, w, lane, barid);
-    }
-  }
+  for (int e = 0; e < E; ++e) buf[w * PW + lane * E + e] = v[e];
   named_bar(barid, 128);
 }
 
-// v (sorted descending) := the K largest of v and another descending list
-// src (K keys, global memory), sorted descending: the elementwise max of v and
-// src reversed is a bitonic sequence holding the K largest, and one bitonic
-// merge sorts it.
-template <int K, bool ROLL>
-__device__ void group_merge_regs(uint64_t (&v)[K / 128], const unsigned long long* src,
-                                 uint64_t* xbuf, int gt, int barid) {
-  constexpr int PW = K / 4;
-  constexpr int E = PW / 32;
+// L := the K largest keys of the sorted lists src(c), c = c0..c1 (global
+// memory, K keys each, descending, written by other CTAs). xbuf (K keys)
+// may be L itself.
+template <int K, typename SrcOf>
+__device__ __forceinline__ void merge_lists(SrcOf src_of, int c0, int c1, uint64_t* L, uint64_t* xbuf, int gt,
+                                            int barid) {
+  constexpr int PW = K / 4, E = PW / 32;
   const int w = gt >> 5, lane = gt & 31;
+  const int x0 = w * PW + lane * E;
+  uint64_t v[E];
+  const unsigned long long* s0 = src_of(c0);
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int x = w * PW + e * 32 + lane;
-    const uint64_t o = __ldcg(src + (K - 1 - x));
-    v[e] = v[e] > o ? v[e] : o;
+  for (int e = 0; e < E; ++e) v[e] = __ldcg(s0 + x0 + e);
+  for (int c = c0 + 1; c <= c1; ++c) {
+    const unsigned long long* sc = src_of(c);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const uint64_t o = __ldcg(sc + (K - 1 - x0 - e));
+      v[e] = v[e] > o ? v[e] : o;
+    }
+    net_merge<K>(v, xbuf, w, lane, barid);
   }
+  named_bar(barid, 128);  // every read of xbuf is done
 #pragma unroll
-  if constexpr (ROLL) {
-#pragma unroll 1
-    for (int stride = K >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
-  } else {
-#pragma unroll
-    for (int stride = K >> 1; stride > 0; stride >>= 1) bitonic_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
-  }
+  for (int e = 0; e < E; ++e) L[x0 + e] = v[e];
   named_bar(barid, 128);
 }
 
-// Write one output row from sorted registers: positions and scores, -1 / -inf
-// for empty slots.
+// One output row from a sorted list: positions and scores, -1 / -inf for
+// empty slots.
 template <int K>
-__device__ __forceinline__ void write_row(const uint64_t (&v)[K / 128], int32_t* oi, float* os, int gt) {
-  constexpr int PW = K / 4;
-  constexpr int E = PW / 32;
-  const int w = gt >> 5, lane = gt & 31;
+__device__ __forceinline__ void write_row(const uint64_t* L, int32_t* oi, float* os, int gt) {
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int x = w * PW + e * 32 + lane;
-    const uint64_t key = v[e];
+  for (int i = 0; i < K / 128; ++i) {
+    const int x = i * 128 + gt;
+    const uint64_t key = L[x];
     oi[x] = key ? key_pos(key) : -1;
     os[x] = key ? key_score(key) : -__int_as_float(0x7f800000);
   }
-}
-
-template <int K>
-__device__ __forceinline__ void write_keys(const uint64_t (&v)[K / 128], unsigned long long* dst, int gt) {
-  constexpr int PW = K / 4;
-  constexpr int E = PW / 32;
-  const int w = gt >> 5, lane = gt & 31;
-#pragma unroll
-  for (int e = 0; e < E; ++e) dst[w * PW + e * 32 + lane] = v[e];
 }
 
 // ------------------------------------------------------------------ the scorer
@@ -1122,25 +1162,27 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     // ---------------------------------------------------------- top-k groups
     // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile (of
     // every other query tile, query 0, when the tiles hold one query): it
-    // filters the staged scores against each query's running threshold,
-    // keeps the survivors in shared memory, compacts them by radix select
-    // when the buffer fills, and at the end of the query tile selects,
-    // sorts and writes the row (or publishes a partial list and, if it is
-    // the last piece, merges them).
+    // filters the staged scores against each query's threshold into its
+    // candidate buffer, bounds the buffer (batch merge or radix select), and
+    // at the end of the query tile leaves the sorted top-k in the first KSEL
+    // slots and writes the row (or publishes the sorted list of its piece of
+    // the keys and, if it is the last piece to finish, merges all pieces).
     const int tg = (warp - C::W_TOPK) >> 2;
     const int gt = threadIdx.x - 32 * (C::W_TOPK + 4 * tg);
     const int barid = 1 + tg;
     uint32_t* hist = sHist + tg * 512;
-    const int g = tg;
     int tile_seq = 0, seg_i = 0;
     Seg s;
     bool stop = false;
     int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
     unsigned long long* partials =
         reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
-    // query jj of this group in the tile, and its running top-k buffer
+    // query jj of this group in the tile, its running top-k and where its
+    // candidates go (the batch after the sorted list, or the whole buffer)
     auto qrow = [&](int jj) { return C::ALT ? jj : tg * C::QPT + jj; };
+    auto qlist = [&](int jj) { return sTopk + (C::ALT ? tg : tg * C::QPT + jj) * C::TK; };
     auto qbuf = [&](int jj) { return C::ALT ? tg : tg * C::QPT + jj; };
+    auto qcand = [&](int jj) { return qlist(jj) + (C::ALT ? KSEL : 0); };
     while (!stop && it.next(s)) {
       if (C::ALT && (seg_i++ & 1) != tg) continue;  // the other group's query tile
       unsigned long long thr[C::QPT];
@@ -1150,6 +1192,11 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         if (gt == 0) {
           ms->cnt[jb] = 0;
           ms->thr[jb] = 0;
+        }
+        if constexpr (C::ALT) {
+          uint64_t* L = qlist(jj);
+#pragma unroll
+          for (int i = 0; i < KSEL / 128; ++i) L[i * 128 + gt] = 0ull;
         }
         thr[jj] = 0;
       }
@@ -1167,7 +1214,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
             const float sc = sSt[st * (QT * kTile) + j * kTile + gt];
             const uint64_t key = make_key(sc, pos);
             const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
-            push_key(pass, key, sTopk + jb * C::CAP, &ms->cnt[jb], lane);
+            push_key(pass, key, qcand(jj), &ms->cnt[jb], lane);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->st_empty[st]);
@@ -1184,8 +1231,14 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
           const int jb = qbuf(jj);
-          if (ms->cnt[jb] > C::CAP - kTile)
-            group_compact(sTopk + jb * C::CAP, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, g, gt, barid);
+          // make room before the next tile could overflow the buffer
+          if constexpr (C::ALT) {
+            if (ms->cnt[jb] > KSEL - kTile)
+              batch_merge<KSEL>(qcand(jj), &ms->cnt[jb], qlist(jj), &ms->thr[jb], gt, barid);
+          } else {
+            if (ms->cnt[jb] > C::TK - kTile)
+              group_compact(qcand(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+          }
           thr[jj] = ms->thr[jb];
         }
         ++tile_seq;
@@ -1193,16 +1246,24 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       if (stop) break;
 
       // ------------------------------------------------ finish the segment
+#pragma unroll
+      for (int jj = 0; jj < C::QPT; ++jj) {
+        const int jb = qbuf(jj);
+        if constexpr (C::ALT) {
+          if (ms->cnt[jb] > 0)
+            batch_merge<KSEL>(qcand(jj), &ms->cnt[jb], qlist(jj), &ms->thr[jb], gt, barid);
+        } else {
+          group_compact(qcand(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+          if (qrow(jj) < s.nrows) sort_list<KSEL>(qlist(jj), min(ms->cnt[jb], KSEL), gt, barid);
+        }
+      }
       if (s.whole) {
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
-          const int j = qrow(jj), jb = qbuf(jj);
-          group_compact(sTopk + jb * C::CAP, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, g, gt, barid);
+          const int j = qrow(jj);
           if (j < s.nrows) {
             const long long o = static_cast<long long>(s.row0 + j) * KSEL;
-            uint64_t v[KSEL / 128];
-            group_sort_regs<KSEL, QT == 1>(sTopk + jb * C::CAP, min(ms->cnt[jb], KSEL), v, gt, barid);
-            write_row<KSEL>(v, a.out_idx + o, a.out_score + o, gt);
+            write_row<KSEL>(qlist(jj), a.out_idx + o, a.out_score + o, gt);
           }
         }
       } else {
@@ -1211,12 +1272,12 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         const int slot = partial_slot(cta, s.qstart, total, Ge);
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
-          const int j = qrow(jj), jb = qbuf(jj);
-          group_compact(sTopk + jb * C::CAP, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, g, gt, barid);
+          const int j = qrow(jj);
           if (j < s.nrows) {
-            uint64_t v[KSEL / 128];
-            group_sort_regs<KSEL, QT == 1>(sTopk + jb * C::CAP, min(ms->cnt[jb], KSEL), v, gt, barid);
-            write_keys<KSEL>(v, partials + (static_cast<long long>(slot) * QT + j) * KSEL, gt);
+            const uint64_t* L = qlist(jj);
+            unsigned long long* dst = partials + (static_cast<long long>(slot) * QT + j) * KSEL;
+#pragma unroll
+            for (int i = 0; i < KSEL / 128; ++i) dst[i * 128 + gt] = L[i * 128 + gt];
           }
         }
         __threadfence();
@@ -1234,20 +1295,15 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         if (ms->glast[tg]) {
 #pragma unroll
           for (int jj = 0; jj < C::QPT; ++jj) {
-            const int j = qrow(jj), jb = qbuf(jj);
+            const int j = qrow(jj);
             if (j < s.nrows) {
-              uint64_t v[KSEL / 128];
-              const unsigned long long* src0 =
-                  partials + (static_cast<long long>(partial_slot(cf, s.qstart, total, Ge)) * QT + j) * KSEL;
-#pragma unroll
-              for (int e = 0; e < KSEL / 128; ++e) v[e] = __ldcg(src0 + (gt >> 5) * (KSEL / 4) + e * 32 + lane);
-              for (int c = cf + 1; c <= cl; ++c) {
-                const unsigned long long* src =
-                    partials + (static_cast<long long>(partial_slot(c, s.qstart, total, Ge)) * QT + j) * KSEL;
-                group_merge_regs<KSEL, QT == 1>(v, src, sTopk + jb * C::CAP, gt, barid);
-              }
+              auto src_of = [&](int c) {
+                return partials + (static_cast<long long>(partial_slot(c, s.qstart, total, Ge)) * QT + j) * KSEL;
+              };
+              uint64_t* L = qlist(jj);
+              merge_lists<KSEL>(src_of, cf, cl, L, L, gt, barid);
               const long long o = static_cast<long long>(s.row0 + j) * KSEL;
-              write_row<KSEL>(v, a.out_idx + o, a.out_score + o, gt);
+              write_row<KSEL>(L, a.out_idx + o, a.out_score + o, gt);
             }
           }
         }
