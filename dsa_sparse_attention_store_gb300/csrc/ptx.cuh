@@ -118,6 +118,15 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// d (+)= a * b with e4m3 A and B (both operands e4m3), fp32 accumulation
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // arrive on an mbarrier once every tcgen05 op issued so far by this thread completes
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
@@ -197,9 +206,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B type
-// (bits 7-9, 10-12: 0 = f16, 1 = bf16), both K-major, N>>3 at [17,23),
-// M>>4 at [24,29).
+// Instruction descriptor: D fp32 (bits 4-5 = 1), A and B type (bits 7-9,
+// 10-12: code 0 = f16 for kind::f16 and e4m3 for kind::f8f6f4, code 1 =
+// bf16 for kind::f16), both K-major, N>>3 at [17,23), M>>4 at [24,29).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);

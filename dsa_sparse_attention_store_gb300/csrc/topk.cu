@@ -6,7 +6,7 @@
 // matrix product), each head's dot product goes through a ReLU, the heads are
 // combined with per-head weights into one score per key, keys after the
 // query's position are masked, and the top-k positions (k = 512 or 1024) are
-// kept. Fp8 keys are up-converted exactly before the product.
+// kept. Fp8 keys enter the product as stored (e4m3 tensor-core operands).
 //
 // Why it streams ("When the Fused Kernel Isn't Enough", section "The
 // Message: Validation and Discovery"): materialising the [q_len x ctx]
@@ -20,9 +20,9 @@
 //   plan    one CTA: query tiles (QT queries of one sequence), a prefix sum
 //           of their key-tile counts, and each CTA's first query tile, so the
 //           CTAs split the total work evenly with one dependent load.
-//   qprep   fp8 caches only: q -> f16 with a power-of-two scale per (query,
-//           head) so the largest magnitude lands in [2^14, 2^15); the scale's
-//           inverse is folded into the head weight (exact).
+//   qprep   fp8 caches only: q -> two e4m3 terms with a power-of-two scale
+//           per (query, head), the scale's inverse folded into the head
+//           weight, so the tensor cores take the stored e4m3 keys as they are.
 //   score   persistent, one CTA per SM, warp-specialised:
 //             warp 0      producer: page-table lookups, TMA of 64-token pages
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
@@ -36,7 +36,6 @@
 //                         selection, sort and output (or, for a query tile
 //                         split across CTAs, a sorted partial list, merged by
 //                         the piece that finishes last)
-//             fp8 only    e4m3 -> f16 conversion of staged key tiles
 //           Keys sit on the MMA's M dimension so each score thread owns one
 //           key (one TMEM lane) and reduces over heads in its own registers.
 #include <cuda_bf16.h>
@@ -271,14 +270,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
 }
 
-// ------------------------------------------------------------------ fp8: queries -> f16
-// One warp per (query, head) row of 128 values. The power-of-two scale
-// 2^e puts the row's largest magnitude in [2^14, 2^15), so every bf16 value
-// within 2^31 of it converts to f16 exactly; w' = w * 2^-e undoes it after
-// the ReLU (relu(2^e x) = 2^e relu(x)).
+// ------------------------------------------------------------------ fp8: queries -> two e4m3 terms
+// Fp8 key tiles go to the tensor cores as they are stored (kind::f8f6f4,
+// e4m3 x e4m3, both operands of one type), so each query row is split into
+// two e4m3 terms whose sum is the bf16 query: one warp per (query, head) row
+// of 128 values; a power-of-two scale 2^e puts the row's largest magnitude
+// in [2^7, 2^8); t1 = e4m3(2^e q) and t2 = e4m3(2^e q - t1), the difference
+// exact in fp32. A bf16 value has 8 significant bits and an e4m3 normal 4,
+// so t1 + t2 = 2^e q exactly whenever the remainder is not below e4m3's
+// subnormal step, i.e. for every value at least 2^-10 of the row's maximum;
+// smaller ones keep an absolute error of at most 2^-10 (scaled units).
+// Products of e4m3 operands are exact in the fp32 accumulator, and
+// w' = w * 2^-e undoes the scale after the ReLU (relu(2^e x) = 2^e relu(x)).
+// Output: t1 rows, then t2 rows, 128 bytes each.
 __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
                                                     const float* __restrict__ w,
-                                                    uint2* __restrict__ qh, float* __restrict__ wq,
+                                                    uint32_t* __restrict__ qe, float* __restrict__ wq,
                                                     long long rows) {
   pdl_wait();
   pdl_trigger();
@@ -295,15 +302,22 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
   if (m > 0.f) {
     int ex;
     frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
-    e = 15 - ex;
+    e = 8 - ex;
   }
-  __half h[4];
+  uint32_t t1 = 0, t2 = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __float2half_rn(ldexpf(x[i], e));
-  uint2 o;
-  o.x = static_cast<uint32_t>(__half_as_ushort(h[0])) | (static_cast<uint32_t>(__half_as_ushort(h[1])) << 16);
-  o.y = static_cast<uint32_t>(__half_as_ushort(h[2])) | (static_cast<uint32_t>(__half_as_ushort(h[3])) << 16);
-  qh[r * 32 + lane] = o;
+  for (int p = 0; p < 2; ++p) {
+    const float y0 = ldexpf(x[2 * p], e), y1 = ldexpf(x[2 * p + 1], e);
+    const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+    const __half2_raw ah = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
+    const float r0 = y0 - __half2float(__ushort_as_half(ah.x));
+    const float r1 = y1 - __half2float(__ushort_as_half(ah.y));
+    const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
+    t1 |= static_cast<uint32_t>(a) << (16 * p);
+    t2 |= static_cast<uint32_t>(b) << (16 * p);
+  }
+  qe[r * 32 + lane] = t1;
+  qe[(rows + r) * 32 + lane] = t2;
   if (lane == 0) wq[r] = ldexpf(w[r], -e);
 }
 
@@ -320,8 +334,8 @@ struct Cfg {
   static constexpr int NTK = ALT ? 2 : QT;
   static constexpr int QPT = ALT ? 1 : QT / NTK;         // queries per top-k group
   static constexpr int NBUF = ALT ? 2 : QT;              // running top-k buffers
-  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 2) : (FMT == DSA_FMT_BF16 ? 5 : 2);
-  static constexpr int SS = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // e4m3 staging
+  // key-tile operand stages (32 KB bf16, 16 KB e4m3)
+  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 6) : (FMT == DSA_FMT_BF16 ? 5 : 8);
   static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
   // alternating groups each read their own ring of staging slots: a group
   // that skips the other's query tile must not wait on a slot phase that
@@ -331,21 +345,17 @@ struct Cfg {
   // keys of one query's running top-k: sorted list + batch of KSEL each
   // (one-query tiles), else a candidate buffer cut back by radix select
   static constexpr int TK = ALT ? 2 * KSEL : 1280;
-  static constexpr int NCONV = FMT == DSA_FMT_FP8 ? (QT == 4 ? 2 : 4) : 0;  // converter warps
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
-  static constexpr int W_CONV = W_TOPK + 4 * NTK;        // first converter warp
-  static constexpr int NWARPS = W_CONV + NCONV;
+  static constexpr int NWARPS = W_TOPK + 4 * NTK;
   static constexpr int NTHREADS = 32 * NWARPS;
   static constexpr int TMEM_COLS = 2 * N;
-  static constexpr int Q_BYTES = N * 256;
-  static constexpr int OP_BYTES = kTile * 256;
-  static constexpr int STG_BYTES = kTile * 128;
+  static constexpr int Q_BYTES = N * 256;                 // bf16, or two e4m3 terms
+  static constexpr int OP_BYTES = kTile * (FMT == DSA_FMT_BF16 ? 256 : 128);
   static constexpr int ST_BYTES = QT * kTile * 4;        // one staged tile of scores
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_OP = OFF_Q + Q_BYTES;
-  static constexpr int OFF_STG = OFF_OP + S * OP_BYTES;
-  static constexpr int OFF_TOPK = OFF_STG + SS * STG_BYTES;
+  static constexpr int OFF_TOPK = OFF_OP + S * OP_BYTES;
   static constexpr int OFF_ST = OFF_TOPK + NBUF * TK * 8;
   static constexpr int OFF_W = OFF_ST + NST * ST_BYTES;
   static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;   // head weights, double-buffered
@@ -358,7 +368,7 @@ struct Cfg {
 };
 
 struct Misc {
-  uint64_t op_full[8], op_empty[8], stg_full[8], stg_empty[8];
+  uint64_t op_full[8], op_empty[8];
   uint64_t tm_full[2], tm_empty[2], q_full, q_empty, fin, w_full[2], w_empty[2];
   uint64_t st_full[16], st_empty[16];
   uint32_t tmem_base;
@@ -378,6 +388,7 @@ struct ScoreArgs {
   const uint8_t* cache;
   int num_pages;
   const float* w;  // head weights (fp8: with the query scale folded in)
+  long long qrows;  // (query, head) rows; fp8: the second e4m3 term's rows follow
   const char* ws;
   WsLayout L;
   int32_t* out_idx;
@@ -818,7 +829,6 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = sm + C::OFF_Q;
   uint8_t* sOp = sm + C::OFF_OP;
-  uint8_t* sStg = sm + C::OFF_STG;
   uint64_t* sTopk = reinterpret_cast<uint64_t*>(sm + C::OFF_TOPK);
   float* sW = reinterpret_cast<float*>(sm + C::OFF_W);
   float* sSt = reinterpret_cast<float*>(sm + C::OFF_ST);
@@ -830,12 +840,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
-      mbar_init(&ms->op_full[i], FMT == DSA_FMT_BF16 ? 1 : C::NCONV);
+      mbar_init(&ms->op_full[i], 1);
       mbar_init(&ms->op_empty[i], 1);
-    }
-    for (int i = 0; i < C::SS; ++i) {
-      mbar_init(&ms->stg_full[i], 1);
-      mbar_init(&ms->stg_empty[i], C::NCONV);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->tm_full[i], 1);
@@ -905,8 +911,13 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           *abort_flag = 1;
         } else {
           mbar_arrive_expect_tx(&ms->q_full, C::Q_BYTES);
-          tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
-          tma_load_2d(sQ + C::N * 128, &tm_q, 64, s.row0 * kH, &ms->q_full);
+          if constexpr (FMT == DSA_FMT_BF16) {  // two 64-column halves
+            tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
+            tma_load_2d(sQ + C::N * 128, &tm_q, 64, s.row0 * kH, &ms->q_full);
+          } else {  // the two e4m3 terms
+            tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
+            tma_load_2d(sQ + C::N * 128, &tm_q, 0, static_cast<int>(a.qrows) + s.row0 * kH, &ms->q_full);
+          }
         }
         // the tile's head-weight rows into the weight buffer the epilogue
         // released two query tiles ago (each buffer has its own barriers, so
@@ -944,14 +955,15 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           const bool v0 = p0 >= 0 && p0 < a.num_pages;
           const bool v1 = p1 >= 0 && p1 < a.num_pages;
           if ((2 * t < npg && !v0) || (2 * t + 1 < npg && !v1)) atomicOr(a.status, DSA_DEV_BOUNDS);
-          if constexpr (FMT == DSA_FMT_BF16) {
-            const int slot = tile_seq % C::S, u = tile_seq / C::S;
-            if (!mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1)) {
-              atomicOr(a.status, DSA_DEV_TIMEOUT);
-              *abort_flag = 1;
-            } else {
+          const int slot = tile_seq % C::S, u = tile_seq / C::S;
+          if (!mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1)) {
+            atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          } else {
+            uint8_t* dst = sOp + slot * C::OP_BYTES;
+            if constexpr (FMT == DSA_FMT_BF16) {
+              // a page = two 64-column halves of 64 keys (128 B rows each)
               mbar_arrive_expect_tx(&ms->op_full[slot], (v0 + v1) * 16384);
-              uint8_t* dst = sOp + slot * C::OP_BYTES;
               if (v0) {
                 tma_load_2d(dst, &tm_k, 0, p0 * 64, &ms->op_full[slot]);
                 tma_load_2d(dst + 16384, &tm_k, 64, p0 * 64, &ms->op_full[slot]);
@@ -960,17 +972,11 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
                 tma_load_2d(dst + 8192, &tm_k, 0, p1 * 64, &ms->op_full[slot]);
                 tma_load_2d(dst + 16384 + 8192, &tm_k, 64, p1 * 64, &ms->op_full[slot]);
               }
-            }
-          } else {
-            const int slot = tile_seq % C::SS, u = tile_seq / C::SS;
-            if (!mbar_wait(&ms->stg_empty[slot], (u & 1) ^ 1)) {
-              atomicOr(a.status, DSA_DEV_TIMEOUT);
-              *abort_flag = 1;
             } else {
-              mbar_arrive_expect_tx(&ms->stg_full[slot], (v0 + v1) * 8192);
-              uint8_t* dst = sStg + slot * C::STG_BYTES;
-              if (v0) tma_load_3d(dst, &tm_k, 0, 0, p0, &ms->stg_full[slot]);
-              if (v1) tma_load_3d(dst + 8192, &tm_k, 0, 0, p1, &ms->stg_full[slot]);
+              // a page = 64 keys x 128 e4m3 bytes, the scales after it stay
+              mbar_arrive_expect_tx(&ms->op_full[slot], (v0 + v1) * 8192);
+              if (v0) tma_load_3d(dst, &tm_k, 0, 0, p0, &ms->op_full[slot]);
+              if (v1) tma_load_3d(dst + 8192, &tm_k, 0, 0, p1, &ms->op_full[slot]);
             }
           }
         }
@@ -980,11 +986,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     }
     // on abort, let this CTA's copies in flight land before the CTA exits
     if (lane == 0 && *abort_flag) {
-      constexpr int R = FMT == DSA_FMT_BF16 ? C::S : C::SS;
-      for (int i = 1; i <= R && tile_seq - i >= 0; ++i) {
+      for (int i = 1; i <= C::S && tile_seq - i >= 0; ++i) {
         const int ts = tile_seq - i;
-        uint64_t* fb = FMT == DSA_FMT_BF16 ? &ms->op_full[ts % R] : &ms->stg_full[ts % R];
-        mbar_wait(fb, (ts / R) & 1, 20000000LL);
+        mbar_wait(&ms->op_full[ts % C::S], (ts / C::S) & 1, 20000000LL);
       }
       mbar_wait(&ms->q_full, (seg_i - 1) & 1, 20000000LL);
       if (seg_i > 0) mbar_wait(&ms->w_full[(seg_i - 1) & 1], ((seg_i - 1) >> 1) & 1, 20000000LL);
@@ -1020,9 +1024,18 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           const uint32_t d = tbase + static_cast<uint32_t>(buf * C::N);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32);
-            const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
-            tc_mma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            if constexpr (FMT == DSA_FMT_BF16) {
+              // K = 16 per step: two 64-column halves of 4 steps (32 B each)
+              const uint64_t ad = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32);
+              const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
+              tc_mma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            } else {
+              // K = 32 per step over one 128-byte row; the two query terms
+              // accumulate into the same scores
+              const uint64_t ad = sw128_desc(a0 + (kk & 3) * 32);
+              const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
+              tc_mma_e4m3(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
           }
           tc_commit(&ms->op_empty[slot]);
           tc_commit(&ms->tm_full[buf]);
@@ -1158,7 +1171,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       if (lane == 0) mbar_arrive(&ms->w_empty[seg_i & 1]);  // this warp is done with the weights
       ++seg_i;
     }
-  } else if (warp < C::W_CONV) {
+  } else {
     // ---------------------------------------------------------- top-k groups
     // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile (of
     // every other query tile, query 0, when the tiles hold one query): it
@@ -1310,61 +1323,6 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       }
       named_bar(barid, 128);
     }
-  } else {
-    // ---------------------------------------------------------- fp8: e4m3 -> f16 converters
-    if constexpr (FMT == DSA_FMT_FP8) {
-      const int ct = threadIdx.x - 32 * C::W_CONV;
-      int tile_seq = 0;
-      Seg s;
-      bool stop = false;
-      while (!stop && it.next(s)) {
-        for (int t = s.t0; t < s.t1; ++t) {
-          const int ss = tile_seq % C::SS, us = tile_seq / C::SS;
-          const int slot = tile_seq % C::S, u = tile_seq / C::S;
-          const bool ok = !*abort_flag && mbar_wait(&ms->stg_full[ss], us & 1) &&
-                          mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1);
-          if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) {
-              *abort_flag = 1;
-              atomicOr(a.status, DSA_DEV_TIMEOUT);
-            }
-            stop = true;
-            break;
-          }
-          const uint8_t* src = sStg + ss * C::STG_BYTES;
-          uint8_t* dst = sOp + slot * C::OP_BYTES;
-#pragma unroll 2
-          for (int itn = 0; itn < 1024 / (32 * C::NCONV); ++itn) {
-            const int idx = itn * (32 * C::NCONV) + ct;
-            const int r = idx >> 3, cb = idx & 7;
-            const uint4 e = *reinterpret_cast<const uint4*>(src + r * 128 + cb * 16);
-            const uint32_t wv[4] = {e.x, e.y, e.z, e.w};
-            uint32_t hv[8];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                  static_cast<__nv_fp8x2_storage_t>(wv[p] & 0xFFFFu), __NV_E4M3);
-              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                  static_cast<__nv_fp8x2_storage_t>(wv[p] >> 16), __NV_E4M3);
-              hv[2 * p] = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-              hv[2 * p + 1] = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-            }
-            const int h = cb >> 2;
-            const int c0 = (cb & 3) * 2;
-            uint8_t* rowp = dst + h * 16384 + r * 128;
-            *reinterpret_cast<uint4*>(rowp + (((c0) ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&ms->op_full[slot]);
-            mbar_arrive(&ms->stg_empty[ss]);
-          }
-          ++tile_seq;
-        }
-      }
-    }
   }
 
   tc_fence_before();
@@ -1414,6 +1372,9 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
                        int32_t B, int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
                        float* out_score, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   (void)ws_bytes;
+  // tensor-map row coordinates are 32-bit: (query, head) rows, and for fp8
+  // both query terms, must stay below 2^31
+  if (static_cast<long long>(Tq) * kH * 2 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(ctx->num_sms, Tq, B, k, fmt);
   char* ws = static_cast<char*>(workspace);
   {
@@ -1435,7 +1396,7 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
     LaunchScope scope(ctx, DSA_K_QPREP, stream);
     if (launch_pdl(qprep_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const uint2*>(q),
-                   head_w, reinterpret_cast<uint2*>(ws + L.qh), reinterpret_cast<float*>(ws + L.wq),
+                   head_w, reinterpret_cast<uint32_t*>(ws + L.qh), reinterpret_cast<float*>(ws + L.wq),
                    rows) != cudaSuccess)
       return DSA_ERR_CUDA;
     qsrc = ws + L.qh;
@@ -1444,14 +1405,22 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
 
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(ctx->encode_tiled);
   CUtensorMap tq, tk;
-  {
+  if (fmt == DSA_FMT_BF16) {  // [rows x 128] bf16, boxes of 64 columns
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD * 2)};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(64 * L.QT)};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tq, fmt == DSA_FMT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-            2, const_cast<void*>(qsrc), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qsrc), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return DSA_ERR_CUDA;
+  } else {  // [2 * rows x 128] e4m3: first terms, then second terms
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(2 * rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(64 * L.QT)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qsrc), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return DSA_ERR_CUDA;
   }
@@ -1470,7 +1439,7 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
     const cuuint32_t box[3] = {128, 64, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return DSA_ERR_CUDA;
   }
@@ -1479,6 +1448,7 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   args.page_table = page_table;
   args.max_pages = max_pages;
   args.causal = causal;
+  args.qrows = rows;
   args.cache = static_cast<const uint8_t*>(cache);
   args.num_pages = num_pages;
   args.w = wsrc;

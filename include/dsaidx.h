@@ -124,7 +124,11 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  * 0..seq_lens[b]-1; k is the stored key (fp8: e4m3 value times its scale).
  * Output row r holds the positions (within the sequence) and fp32 scores of
  * the min(k, visible) best keys, ordered by (score desc, position asc);
- * unused slots are -1 / -inf.
+ * unused slots are -1 / -inf. Products accumulate in fp32. For fp8 caches
+ * the stored e4m3 keys enter the tensor cores as they are and each query row
+ * (one head) as two e4m3 terms under a power-of-two scale: exact for every
+ * query value of at least 2^-10 of its row's largest magnitude, smaller
+ * values off by at most 2^-17 of that magnitude.
  *  q           (device) [Tq][64][128] bf16, 16-byte aligned.
  *  head_w      (device) [Tq][64] fp32, 16-byte aligned.
  *  cache       (device) as written by dsa_index_store, num_pages pages of fmt.
@@ -132,7 +136,7 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  *              page are not read.
  *  seq_lens    (device) [B] int32, n_q(b) <= seq_lens[b] <= 64*max_pages.
  *  cu_q        (device) [B+1] int32, cu_q[0] = 0, non-decreasing, cu_q[B] = Tq.
- *  k           512 or 1024.  B <= 16384 (else DSA_ERR_UNSUPPORTED).
+ *  k           512 or 1024.  B <= 16384, Tq < 2^24 (else DSA_ERR_UNSUPPORTED).
  *  out_idx     (device) [Tq][k] int32;  out_score (device) [Tq][k] fp32.
  *  workspace   (device) >= dsa_index_topk_workspace_size(...) bytes, 256-byte
  *              aligned; contents need not be initialised and are scratch.
