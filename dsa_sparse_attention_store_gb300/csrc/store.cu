@@ -43,11 +43,22 @@ __global__ void __launch_bounds__(256) store_kernel(
   const int l = threadIdx.x & 15;
   const bool live = tok < T;
 
+  // Loads in two dependent rounds: the token's raw key, position, sequence
+  // and this lane's gamma first (independent), then its page id and RoPE
+  // row (which need the position and sequence).
   int pos = 0, page = -1;
   bool ok = false;
+  uint4 raw = make_uint4(0, 0, 0, 0);
+  float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+  int s = -1;
   if (live) {
+    raw = k_raw[static_cast<long long>(tok) * 16 + l];
     pos = rope_pos[tok];
-    const int s = seq_id[tok];
+    s = seq_id[tok];
+  }
+  g0 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * l);
+  g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * l + 1);
+  if (live) {
     ok = s >= 0 && s < B && pos >= 0 && pos < max_pos && pos < max_pages * kPage;
     if (ok) {
       page = page_table[static_cast<long long>(s) * max_pages + pos / kPage];
@@ -55,9 +66,13 @@ __global__ void __launch_bounds__(256) store_kernel(
     }
     if (!ok && l == 0) atomicOr(status, DSA_DEV_BOUNDS);
   }
+  const bool pos_ok = live && pos >= 0 && pos < max_pos;  // the RoPE row may be read
+  const float4* cs4 =
+      reinterpret_cast<const float4*>(rope + static_cast<long long>(pos_ok ? pos : 0) * 64 + 8 * (l & 7));
+  float4 cst[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) cst[v] = __ldg(cs4 + v);
 
-  uint4 raw = make_uint4(0, 0, 0, 0);
-  if (ok) raw = k_raw[static_cast<long long>(tok) * 16 + l];
   float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
                 bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
 
@@ -70,32 +85,31 @@ __global__ void __launch_bounds__(256) store_kernel(
   const float ms = __fmul_rn(ss, 0.0078125f);
   const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 
+  const float gm[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   float y[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], r), gamma[8 * l + e]);
+  for (int e = 0; e < 8; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], r), gm[e]);
 
   // RoPE, dims i and i+64 (lanes l and l^8)
   float py[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) py[e] = __shfl_xor_sync(0xffffffffu, y[e], 8);
-  const float4* cs4 =
-      reinterpret_cast<const float4*>(rope + static_cast<long long>(ok ? pos : 0) * 64 + 8 * (l & 7));
-  float c[8], s[8];
+  float c[8], sn[8];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    const float4 t = ok ? __ldg(cs4 + v) : make_float4(1.f, 0.f, 1.f, 0.f);
+    const float4 t = ok ? cst[v] : make_float4(1.f, 0.f, 1.f, 0.f);
     c[2 * v] = t.x;
-    s[2 * v] = t.y;
+    sn[2 * v] = t.y;
     c[2 * v + 1] = t.z;
-    s[2 * v + 1] = t.w;
+    sn[2 * v + 1] = t.w;
   }
   float o[8];
   if (l < 8) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = __fsub_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], s[e]));
+    for (int e = 0; e < 8; ++e) o[e] = __fsub_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], sn[e]));
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], s[e]));
+    for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], sn[e]));
   }
 
   const int off = pos & (kPage - 1);
