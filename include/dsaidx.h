@@ -182,11 +182,10 @@ dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_
 typedef enum {
   DSA_K_STORE = 0,      /* dsa_index_store */
   DSA_K_PLAN = 1,       /* dsa_index_topk: schedule */
-  DSA_K_QPREP = 2,      /* dsa_index_topk, fp8 only: query conversion */
+  DSA_K_QPREP = 2,      /* dsa_index_topk, fp8 only: queries -> two e4m3 terms */
   DSA_K_SCORE_BF16 = 3, /* dsa_index_topk: tensor-core scorer + running top-k, bf16 cache */
   DSA_K_SCORE_FP8 = 4,  /* the same, fp8 cache */
-  DSA_K_SORT = 5,       /* dsa_index_topk: per-row sort */
-  DSA_K_COUNT = 6
+  DSA_K_COUNT = 5
 } dsa_kernel_kind;
 dsa_status dsa_profile_enable(dsa_ctx* ctx, int on);
 dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms /* [DSA_K_COUNT] */,
