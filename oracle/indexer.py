@@ -18,6 +18,11 @@ float64 sums), the ReLU and head sum are float64, and the result is selected
 on those float64 values. Top-k = the first min(k, visible) keys in the order
 (score descending, position ascending); unused slots hold -1 / -inf. Scores
 are reported rounded to fp32.
+
+With a Hadamard-rotated cache (see oracle.store) the stored key is H k; the
+query heads are rotated by the same matrix (float64, exact for bf16 input)
+and the dot products divided by 128, so the scores are those of the
+unrotated vectors up to the store's rounding.
 """
 from __future__ import annotations
 
@@ -45,10 +50,20 @@ def visible_count(cu_q, seq_lens, row: int, causal: bool) -> int:
     return query_position(cu_q, seq_lens, row) + 1 if causal else int(seq_lens[b])
 
 
-def scores(keys: np.ndarray, q_bits: np.ndarray, w: np.ndarray) -> np.ndarray:
+def sylvester(n: int = S.D) -> np.ndarray:
+    """Sylvester Hadamard matrix of order n (entries +-1), float64."""
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def scores(keys: np.ndarray, q_bits: np.ndarray, w: np.ndarray, hadamard: bool = False) -> np.ndarray:
     """float64 scores of keys [n,128] for queries q_bits [m,64,128], w [m,64] -> [m,n]."""
     m = q_bits.shape[0]
     qf = F.bf16_to_f64(q_bits).reshape(m * H, S.D)
+    if hadamard:
+        qf = (qf @ sylvester().T) / 128.0
     dots = keys @ qf.T                                   # [n, m*64]
     dots = np.maximum(dots, 0.0).reshape(keys.shape[0], m, H)
     return np.einsum("nmh,mh->mn", dots, np.asarray(w, dtype=np.float64))
@@ -75,7 +90,8 @@ def select_topk(s: np.ndarray, k: int):
 
 
 def index_topk(cache, fmt, page_table, seq_lens, cu_q, q_bits, head_w, causal: bool,
-               k: int, rows=None, block: int = 16, return_scores: bool = False):
+               k: int, rows=None, block: int = 16, return_scores: bool = False,
+               hadamard: bool = False):
     """Top-k positions and fp32 scores for the given query rows (all by default).
 
     Returns (idx [n, k] int32, score [n, k] float32) and, when return_scores,
@@ -94,7 +110,7 @@ def index_topk(cache, fmt, page_table, seq_lens, cu_q, q_bits, head_w, causal: b
         for c0 in range(0, len(mine), block):
             blk = mine[c0:c0 + block]
             rr = rows[blk]
-            sc = scores(keys, q_bits[rr], head_w[rr])
+            sc = scores(keys, q_bits[rr], head_w[rr], hadamard)
             for t, r in enumerate(rr.tolist()):
                 n = visible_count(cu_q, seq_lens, r, causal)
                 sv = sc[t, :n]

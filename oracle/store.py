@@ -33,6 +33,18 @@ the definition the stored bytes are compared against:
 The 1e-4 floor on amax is this library's reading for an all-zero key (the
 pages do not say); it keeps the scale positive, which the scorer relies on.
 
+Optional Hadamard rotation ("The Moment of Validation", section "Input
+Knowledge Required to Understand This Message": the fused kernel applies a
+Hadamard transform between RoPE and the store; "The Fused Kernel Decision",
+section "Assumptions and Their Validity": queries and keys must come out in
+the same order). The pages fix neither the normalisation nor the order; the
+reading taken here is the unnormalised 128-point Walsh-Hadamard transform in
+natural (Sylvester) order, applied to y' before quantisation:
+    stages h = 1, 2, 4, ..., 64: every pair (i, i+h) with i & h == 0
+    becomes (a + b, a - b), each sum rounded to fp32.
+Its matrix H has entries +-1 and H H^T = 128 I, so a query rotated the same
+way gives (H q) . (H k) = 128 (q . k); the scorer divides by 128 (exact).
+
 Cache layouts (per page of 64 tokens):
   bf16 : [64][128] bf16                         16384 bytes
   fp8  : [64][128] e4m3, then [64] fp32 scales   8448 bytes
@@ -99,14 +111,32 @@ def rope_f32(y: np.ndarray, c: np.ndarray, s: np.ndarray) -> np.ndarray:
     return out
 
 
+def wht_f32(y: np.ndarray) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform of fp32 rows [T,128], natural
+    order, butterfly stages h = 1, 2, ..., 64 with fp32 sums."""
+    y = np.array(y, dtype=np.float32, copy=True)
+    T = y.shape[0]
+    h = 1
+    while h < D:
+        v = y.reshape(T, D // (2 * h), 2, h)
+        a = v[:, :, 0, :].copy()
+        b = v[:, :, 1, :].copy()
+        v[:, :, 0, :] = a + b
+        v[:, :, 1, :] = a - b
+        h *= 2
+    return y
+
+
 def normalize_rotate(k_raw_bits: np.ndarray, pos: np.ndarray, theta: float, eps: float,
-                     gamma_bits: np.ndarray | None = None) -> np.ndarray:
-    """fp32 y' for bf16 raw keys [T,128] at positions pos [T]."""
+                     gamma_bits: np.ndarray | None = None, hadamard: bool = False) -> np.ndarray:
+    """fp32 y' (then H y' when hadamard) for bf16 raw keys [T,128] at
+    positions pos [T]."""
     x = F.bf16_to_f64(k_raw_bits).astype(np.float32)
     gamma = None if gamma_bits is None else F.bf16_to_f64(gamma_bits).astype(np.float32)
     y = rmsnorm_f32(x, eps, gamma)
     c, s = rope_cos_sin(theta, pos)
-    return rope_f32(y, c, s)
+    yr = rope_f32(y, c, s)
+    return wht_f32(yr) if hadamard else yr
 
 
 def quantize_fp8(yr: np.ndarray):
@@ -145,11 +175,11 @@ def _views(cache: np.ndarray, fmt: int):
 
 
 def store(cache: np.ndarray, fmt: int, k_raw_bits, pos, seq, page_table, num_pages: int,
-          theta: float = 10000.0, eps: float = 1e-6, gamma_bits=None) -> None:
+          theta: float = 10000.0, eps: float = 1e-6, gamma_bits=None, hadamard: bool = False) -> None:
     """Write the tokens' index keys into the byte image of the paged cache."""
     if len(pos) == 0:
         return
-    yr = normalize_rotate(k_raw_bits, pos, theta, eps, gamma_bits)
+    yr = normalize_rotate(k_raw_bits, pos, theta, eps, gamma_bits, hadamard)
     page, off = slots(pos, seq, page_table, num_pages)
     data, scales = _views(cache, fmt)
     if fmt == FMT_BF16:
