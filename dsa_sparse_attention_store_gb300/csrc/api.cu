@@ -120,6 +120,12 @@ dsa_status dsa_ctx_destroy(dsa_ctx* ctx) {
   return DSA_OK;
 }
 
+dsa_status dsa_ctx_set_hadamard(dsa_ctx* ctx, int32_t on) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  ctx->hadamard = on ? 1 : 0;
+  return DSA_OK;
+}
+
 dsa_status dsa_profile_enable(dsa_ctx* ctx, int on) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
   if (on && !ctx->prof) {

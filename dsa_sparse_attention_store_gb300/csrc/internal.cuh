@@ -24,6 +24,7 @@ struct dsa_ctx {
   float eps;
   int max_pos;
   float2* rope;          // [max_pos][64] (cos, sin), fp32
+  int hadamard;          // store keys rotated by the 128-point Walsh-Hadamard transform
   float* gamma;          // [128]
   unsigned int* status;  // device status word
   void* encode_tiled;    // cuTensorMapEncodeTiled entry point

@@ -17,6 +17,12 @@
 // reproducible. RoPE pairs dim i (lane l < 8) with dim i+64 (lane l+8), one
 // shuffle. Every fp32 step uses the round-to-nearest intrinsics so no
 // multiply-add is contracted.
+//
+// Optional Hadamard rotation (same pages: the fused kernel applies a Hadamard
+// transform before the store): the unnormalised 128-point Walsh-Hadamard
+// transform in natural order, as butterflies h = 1, 2, 4 inside a lane's 8
+// dims and h = 8, 16, 32, 64 between lanes l and l ^ (h/8), each pair
+// (i, i+h) becoming (a + b, a - b) in fp32.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -31,7 +37,7 @@ constexpr int kPage = 64;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-template <int FMT>
+template <int FMT, bool HAD>
 __global__ void __launch_bounds__(256) store_kernel(
     const uint4* __restrict__ k_raw, const int32_t* __restrict__ rope_pos,
     const int32_t* __restrict__ seq_id, const int32_t* __restrict__ page_table, int T, int B,
@@ -112,6 +118,28 @@ __global__ void __launch_bounds__(256) store_kernel(
     for (int e = 0; e < 8; ++e) o[e] = __fadd_rn(__fmul_rn(y[e], c[e]), __fmul_rn(py[e], sn[e]));
   }
 
+  if constexpr (HAD) {
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if ((e & h) == 0) {
+          const float a = o[e], b = o[e + h];
+          o[e] = __fadd_rn(a, b);
+          o[e + h] = __fsub_rn(a, b);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float p = __shfl_xor_sync(0xffffffffu, o[e], m);
+        o[e] = (l & m) ? __fsub_rn(p, o[e]) : __fadd_rn(o[e], p);
+      }
+    }
+  }
+
   const int off = pos & (kPage - 1);
   if constexpr (FMT == DSA_FMT_BF16) {
     if (ok) {
@@ -162,7 +190,8 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
   const long long threads = static_cast<long long>(T) * 16;
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   LaunchScope scope(ctx, DSA_K_STORE, stream);
-  auto kern = fmt == DSA_FMT_BF16 ? store_kernel<DSA_FMT_BF16> : store_kernel<DSA_FMT_FP8>;
+  auto kern = fmt == DSA_FMT_BF16 ? (ctx->hadamard ? store_kernel<DSA_FMT_BF16, true> : store_kernel<DSA_FMT_BF16, false>)
+                                  : (ctx->hadamard ? store_kernel<DSA_FMT_FP8, true> : store_kernel<DSA_FMT_FP8, false>);
   const cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, stream,
                                    static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B,
                                    max_pages, static_cast<uint8_t*>(cache), num_pages,

@@ -76,7 +76,7 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 inline int pick_qt(int Tq, int B) { return (Tq >= 2 * B && Tq >= 4) ? 4 : 1; }
 
-WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
+WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
   WsLayout L{};
   L.QT = pick_qt(Tq, B);
   L.NG = L.QT;  // top-k groups (one per query): merge counters per (query tile, group)
@@ -95,7 +95,7 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt) {
   o = up256(o + static_cast<size_t>(L.G) * 4);
   L.partials = o;
   o = up256(o + static_cast<size_t>(2) * L.G * L.QT * k * 8);
-  if (fmt == DSA_FMT_FP8) {
+  if (fmt == DSA_FMT_FP8 || hadamard) {  // prepared queries and head weights
     L.qh = o;
     o = up256(o + static_cast<size_t>(Tq) * kH * kD * 2);
     L.wq = o;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
 }
 
-// ------------------------------------------------------------------ fp8: queries -> two e4m3 terms
+// ------------------------------------------------------------------ query preparation
 // Fp8 key tiles go to the tensor cores as they are stored (kind::f8f6f4,
 // e4m3 x e4m3, both operands of one type), so each query row is split into
 // two e4m3 terms whose sum is the bf16 query: one warp per (query, head) row
@@ -283,6 +283,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 // Products of e4m3 operands are exact in the fp32 accumulator, and
 // w' = w * 2^-e undoes the scale after the ReLU (relu(2^e x) = 2^e relu(x)).
 // Output: t1 rows, then t2 rows, 128 bytes each.
+//
+// With the Hadamard rotation on, the row is first rotated by the same
+// unnormalised Walsh-Hadamard transform as the stored keys (fp32 butterflies
+// in the store's order: h = 1, 2 inside a lane's 4 values, h = 4 .. 64
+// between lanes l and l ^ (h/4)) and rounded to bf16, and w' carries a
+// further 2^-7 (the transform's gain 128 on the dot product); bf16 caches
+// take the rotated bf16 row as it is (E4M3 = false: 256-byte rows).
+template <bool E4M3, bool HAD>
 __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
                                                     const float* __restrict__ w,
                                                     uint32_t* __restrict__ qe, float* __restrict__ wq,
@@ -295,30 +303,65 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
   const uint2 v = q[r * 32 + lane];
   float x[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
                 __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)};
-  float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  if constexpr (HAD) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  int e = 0;
-  if (m > 0.f) {
-    int ex;
-    frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
-    e = 8 - ex;
-  }
-  uint32_t t1 = 0, t2 = 0;
+    for (int h = 1; h < 4; h <<= 1) {
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    const float y0 = ldexpf(x[2 * p], e), y1 = ldexpf(x[2 * p + 1], e);
-    const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
-    const __half2_raw ah = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
-    const float r0 = y0 - __half2float(__ushort_as_half(ah.x));
-    const float r1 = y1 - __half2float(__ushort_as_half(ah.y));
-    const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
-    t1 |= static_cast<uint32_t>(a) << (16 * p);
-    t2 |= static_cast<uint32_t>(b) << (16 * p);
+      for (int e = 0; e < 4; ++e) {
+        if ((e & h) == 0) {
+          const float a = x[e], b = x[e + h];
+          x[e] = __fadd_rn(a, b);
+          x[e + h] = __fsub_rn(a, b);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = __shfl_xor_sync(0xffffffffu, x[e], m);
+        x[e] = (lane & m) ? __fsub_rn(p, x[e]) : __fadd_rn(x[e], p);
+      }
+    }
+    // the rotated query is a bf16 operand, like the plain one
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
   }
-  qe[r * 32 + lane] = t1;
-  qe[(rows + r) * 32 + lane] = t2;
-  if (lane == 0) wq[r] = ldexpf(w[r], -e);
+  constexpr int kGain = HAD ? 7 : 0;  // log2 of the rotation's gain on q . k
+  if constexpr (!E4M3) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&lo);
+    o.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(qe)[r * 32 + lane] = o;
+    if (lane == 0) wq[r] = ldexpf(w[r], -kGain);
+  } else {
+    float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    int e = 0;
+    if (m > 0.f) {
+      int ex;
+      frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
+      e = 8 - ex;
+    }
+    uint32_t t1 = 0, t2 = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const float y0 = ldexpf(x[2 * p], e), y1 = ldexpf(x[2 * p + 1], e);
+      const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw ah = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
+      const float r0 = y0 - __half2float(__ushort_as_half(ah.x));
+      const float r1 = y1 - __half2float(__ushort_as_half(ah.y));
+      const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
+      t1 |= static_cast<uint32_t>(a) << (16 * p);
+      t2 |= static_cast<uint32_t>(b) << (16 * p);
+    }
+    qe[r * 32 + lane] = t1;
+    qe[(rows + r) * 32 + lane] = t2;
+    if (lane == 0) wq[r] = ldexpf(w[r], -e - kGain);
+  }
 }
 
 // ------------------------------------------------------------------ scorer configuration
@@ -1363,7 +1406,7 @@ dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtenso
 int max_sequences() { return kMaxSeqs; }
 
 size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt) {
-  return ws_layout(ctx->num_sms, Tq, B, k, fmt).total;
+  return ws_layout(ctx->num_sms, Tq, B, k, fmt, ctx->hadamard != 0).total;
 }
 
 dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
@@ -1375,7 +1418,7 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   // tensor-map row coordinates are 32-bit: (query, head) rows, and for fp8
   // both query terms, must stay below 2^31
   if (static_cast<long long>(Tq) * kH * 2 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, k, fmt);
+  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, k, fmt, ctx->hadamard != 0);
   char* ws = static_cast<char*>(workspace);
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
@@ -1392,10 +1435,13 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   const void* qsrc = q;
   const float* wsrc = head_w;
   const long long rows = static_cast<long long>(Tq) * kH;
-  if (fmt == DSA_FMT_FP8) {
+  if (fmt == DSA_FMT_FP8 || ctx->hadamard) {
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
     LaunchScope scope(ctx, DSA_K_QPREP, stream);
-    if (launch_pdl(qprep_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const uint2*>(q),
+    const bool e4 = fmt == DSA_FMT_FP8;
+    auto kern = ctx->hadamard ? (e4 ? qprep_kernel<true, true> : qprep_kernel<false, true>)
+                              : qprep_kernel<true, false>;
+    if (launch_pdl(kern, dim3(blocks), dim3(256), 0, stream, static_cast<const uint2*>(q),
                    head_w, reinterpret_cast<uint32_t*>(ws + L.qh), reinterpret_cast<float*>(ws + L.wq),
                    rows) != cudaSuccess)
       return DSA_ERR_CUDA;

@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.dsa_index_topk_static.restype = ctypes.c_int
         L.dsa_get_device_status.argtypes = [_c_ptr, _c_ptr]
         L.dsa_get_device_status.restype = ctypes.c_int
+        L.dsa_ctx_set_hadamard.argtypes = [_c_ptr, _c_int]
+        L.dsa_ctx_set_hadamard.restype = ctypes.c_int
         L.dsa_profile_enable.argtypes = [_c_ptr, ctypes.c_int]
         L.dsa_profile_enable.restype = ctypes.c_int
         L.dsa_profile_read.argtypes = [_c_ptr, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_c_int)]
@@ -196,6 +198,12 @@ class Context:
             _dev(out_score, torch.float32, (Tq, k), "out_score"), _stream_ptr(stream))
         if st != 0:
             raise DsaError("dsa_index_topk_static", st)
+
+    def set_hadamard(self, on: bool = True):
+        """Store keys (and rotate queries) with the 128-point Walsh-Hadamard transform."""
+        st = lib().dsa_ctx_set_hadamard(self._h, 1 if on else 0)
+        if st != 0:
+            raise DsaError("dsa_ctx_set_hadamard", st)
 
     def profile_enable(self, on: bool = True):
         st = lib().dsa_profile_enable(self._h, 1 if on else 0)

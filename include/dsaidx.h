@@ -110,6 +110,23 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
                            int32_t B, int32_t max_pages, void* cache, int32_t num_pages,
                            dsa_fmt fmt, dsa_stream_t stream);
 
+/* Hadamard rotation ("The Moment of Validation", section "Input Knowledge
+ * Required to Understand This Message": the fused store applies a Hadamard
+ * transform between RoPE and quantisation; "The Fused Kernel Decision",
+ * section "Assumptions and Their Validity": queries and keys must use the
+ * same order). When on, dsa_index_store writes H y' instead of y', H the
+ * unnormalised 128-point Walsh-Hadamard transform in natural (Sylvester)
+ * order (entries +-1, fp32 butterflies h = 1, 2, ..., 64, each pair
+ * (i, i+h) -> (a + b, a - b)), and dsa_index_topk rotates every query head by
+ * the same H and divides the dot products by 128, so scores keep their
+ * meaning: (H q) . (H k) / 128 = q . k. The rotated query is rounded to bf16,
+ * the precision of the plain query (fp8 caches then split it into two e4m3
+ * terms as usual).
+ * A cache must be written and read with the same setting. Off by default;
+ * applies to the calls made after it, and changes the size
+ * dsa_index_topk_workspace_size reports for bf16 caches. */
+dsa_status dsa_ctx_set_hadamard(dsa_ctx* ctx, int32_t on);
+
 /* Upper bound of the workspace bytes dsa_index_topk needs for these sizes.
  * It does not grow with the context length: it holds the schedule
  * (O(Tq + B)), split-context partial lists (O(#SMs * k)) and, for fp8
@@ -182,7 +199,7 @@ dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_
 typedef enum {
   DSA_K_STORE = 0,      /* dsa_index_store */
   DSA_K_PLAN = 1,       /* dsa_index_topk: schedule */
-  DSA_K_QPREP = 2,      /* dsa_index_topk, fp8 only: queries -> two e4m3 terms */
+  DSA_K_QPREP = 2,      /* dsa_index_topk, fp8 or Hadamard: query preparation */
   DSA_K_SCORE_BF16 = 3, /* dsa_index_topk: tensor-core scorer + running top-k, bf16 cache */
   DSA_K_SCORE_FP8 = 4,  /* the same, fp8 cache */
   DSA_K_COUNT = 5

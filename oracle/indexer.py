@@ -19,10 +19,11 @@ on those float64 values. Top-k = the first min(k, visible) keys in the order
 (score descending, position ascending); unused slots hold -1 / -inf. Scores
 are reported rounded to fp32.
 
-With a Hadamard-rotated cache (see oracle.store) the stored key is H k; the
-query heads are rotated by the same matrix (float64, exact for bf16 input)
-and the dot products divided by 128, so the scores are those of the
-unrotated vectors up to the store's rounding.
+With a Hadamard-rotated cache (see oracle.store) the stored key is H k; each
+query head is rotated by the same fp32 butterflies and rounded to bf16 (the
+rotated query is a bf16 operand, like the plain one), and the dot products
+are divided by 128 (exact), so the scores are those of the unrotated vectors
+up to the store's and the query's rounding.
 """
 from __future__ import annotations
 
@@ -63,7 +64,8 @@ def scores(keys: np.ndarray, q_bits: np.ndarray, w: np.ndarray, hadamard: bool =
     m = q_bits.shape[0]
     qf = F.bf16_to_f64(q_bits).reshape(m * H, S.D)
     if hadamard:
-        qf = (qf @ sylvester().T) / 128.0
+        qr = S.wht_f32(qf.astype(np.float32))              # exact input: bf16 -> fp32
+        qf = F.bf16_to_f64(F.f32_to_bf16(qr)) / 128.0
     dots = keys @ qf.T                                   # [n, m*64]
     dots = np.maximum(dots, 0.0).reshape(keys.shape[0], m, H)
     return np.einsum("nmh,mh->mn", dots, np.asarray(w, dtype=np.float64))

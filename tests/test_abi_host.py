@@ -75,6 +75,8 @@ def test_invalid_arguments_rejected_without_device(L):
     assert L.dsa_index_topk_workspace_size(fake, 4, 1, 300, 0) == 0
     assert L.dsa_index_topk_workspace_size(None, 4, 1, 512, 0) == 0
     assert L.dsa_index_topk_workspace_size(fake, 4, 1, 512, 9) == 0
+    # settings on a null context
+    assert L.dsa_ctx_set_hadamard(None, 1) == 1
 
 
 def test_context_creation_without_gpu_fails_cleanly(L):

@@ -95,13 +95,13 @@ def test_bruteforce_tiny_rotated():
     oi, os_ = X.index_topk(cache, S.FMT_BF16, wl.page_table, wl.seq_lens, wl.cu_q, wl.q,
                            wl.head_w, True, 8, hadamard=True)
     keys = S.read_keys(cache, S.FMT_BF16, wl.page_table[0], 90).tolist()
-    Hm = X.sylvester().tolist()
     for r in range(wl.Tq):
         qpos = 90 - 3 + r
         qv = F.bf16_to_f64(wl.q[r]).tolist()
         w = [float(v) for v in wl.head_w[r]]
-        # the query heads rotated by the explicit matrix, one head at a time
-        qr = [[sum(Hm[i][j] * qv[h][j] for j in range(128)) for i in range(128)] for h in range(64)]
+        # the query heads rotated (fp32 butterflies, pinned above) and rounded
+        # to bf16, the rotated query's precision
+        qr = F.bf16_to_f64(F.f32_to_bf16(S.wht_f32(np.asarray(qv, dtype=np.float32)))).tolist()
         sc = []
         for p in range(qpos + 1):
             tot = 0.0
