@@ -25,6 +25,7 @@ struct dsa_ctx {
   int max_pos;
   float2* rope;          // [max_pos][64] (cos, sin), fp32
   int hadamard;          // store keys rotated by the 128-point Walsh-Hadamard transform
+  int slot_output;       // top-k returns cache slots instead of positions
   float* gamma;          // [128]
   unsigned int* status;  // device status word
   void* encode_tiled;    // cuTensorMapEncodeTiled entry point

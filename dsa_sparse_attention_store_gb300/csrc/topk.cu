@@ -75,6 +75,8 @@ struct WsLayout {
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 inline int pick_qt(int Tq, int B) { return (Tq >= 2 * B && Tq >= 4) ? 4 : 1; }
+// selection size (the sorting networks' K) for an output of k entries
+inline int select_size(int k) { return k <= 512 ? 512 : 1024; }
 
 WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
   WsLayout L{};
@@ -436,6 +438,8 @@ struct ScoreArgs {
   WsLayout L;
   int32_t* out_idx;
   float* out_score;
+  int kout;         // entries per output row (<= the selection size KSEL)
+  int slots;        // output cache slots instead of positions
   unsigned int* status;
 };
 
@@ -849,16 +853,25 @@ __device__ __forceinline__ void merge_lists(SrcOf src_of, int c0, int c1, uint64
   named_bar(barid, 128);
 }
 
-// One output row from a sorted list: positions and scores, -1 / -inf for
-// empty slots.
+// One output row from a sorted list: its first kout entries, positions (or
+// cache slots, page_table[pos / 64] * 64 + pos % 64, when pt_row is given)
+// and scores, -1 / -inf for empty slots.
 template <int K>
-__device__ __forceinline__ void write_row(const uint64_t* L, int32_t* oi, float* os, int gt) {
+__device__ __forceinline__ void write_row(const uint64_t* L, int32_t* oi, float* os, int kout,
+                                          const int32_t* pt_row, int gt) {
 #pragma unroll
   for (int i = 0; i < K / 128; ++i) {
     const int x = i * 128 + gt;
-    const uint64_t key = L[x];
-    oi[x] = key ? key_pos(key) : -1;
-    os[x] = key ? key_score(key) : -__int_as_float(0x7f800000);
+    if (x < kout) {
+      const uint64_t key = L[x];
+      int id = -1;
+      if (key) {
+        const int pos = key_pos(key);
+        id = pt_row ? pt_row[pos >> 6] * 64 + (pos & 63) : pos;
+      }
+      oi[x] = id;
+      os[x] = key ? key_score(key) : -__int_as_float(0x7f800000);
+    }
   }
 }
 
@@ -1239,6 +1252,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
     auto qlist = [&](int jj) { return sTopk + (C::ALT ? tg : tg * C::QPT + jj) * C::TK; };
     auto qbuf = [&](int jj) { return C::ALT ? tg : tg * C::QPT + jj; };
     auto qcand = [&](int jj) { return qlist(jj) + (C::ALT ? KSEL : 0); };
+    // page-table row for slot output (null: positions)
+    auto out_pt = [&](const Seg& sg) -> const int32_t* {
+      return a.slots ? a.page_table + static_cast<long long>(sg.b) * a.max_pages : nullptr;
+    };
     while (!stop && it.next(s)) {
       if (C::ALT && (seg_i++ & 1) != tg) continue;  // the other group's query tile
       unsigned long long thr[C::QPT];
@@ -1318,8 +1335,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         for (int jj = 0; jj < C::QPT; ++jj) {
           const int j = qrow(jj);
           if (j < s.nrows) {
-            const long long o = static_cast<long long>(s.row0 + j) * KSEL;
-            write_row<KSEL>(qlist(jj), a.out_idx + o, a.out_score + o, gt);
+            const long long o = static_cast<long long>(s.row0 + j) * a.kout;
+            write_row<KSEL>(qlist(jj), a.out_idx + o, a.out_score + o, a.kout, out_pt(s), gt);
           }
         }
       } else {
@@ -1358,8 +1375,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
               };
               uint64_t* L = qlist(jj);
               merge_lists<KSEL>(src_of, cf, cl, L, L, gt, barid);
-              const long long o = static_cast<long long>(s.row0 + j) * KSEL;
-              write_row<KSEL>(L, a.out_idx + o, a.out_score + o, gt);
+              const long long o = static_cast<long long>(s.row0 + j) * a.kout;
+              write_row<KSEL>(L, a.out_idx + o, a.out_score + o, a.kout, out_pt(s), gt);
             }
           }
         }
@@ -1406,7 +1423,7 @@ dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtenso
 int max_sequences() { return kMaxSeqs; }
 
 size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt) {
-  return ws_layout(ctx->num_sms, Tq, B, k, fmt, ctx->hadamard != 0).total;
+  return ws_layout(ctx->num_sms, Tq, B, select_size(k), fmt, ctx->hadamard != 0).total;
 }
 
 dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
@@ -1418,7 +1435,10 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   // tensor-map row coordinates are 32-bit: (query, head) rows, and for fp8
   // both query terms, must stay below 2^31
   if (static_cast<long long>(Tq) * kH * 2 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, k, fmt, ctx->hadamard != 0);
+  // any k <= 1024 runs the top-512 or top-1024 selection and writes the
+  // first k entries of each sorted row
+  const int ksel = select_size(k);
+  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, ksel, fmt, ctx->hadamard != 0);
   char* ws = static_cast<char*>(workspace);
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
@@ -1501,14 +1521,16 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   args.ws = ws;
   args.L = L;
   args.out_idx = out_idx;
+  args.kout = k;
+  args.slots = ctx->slot_output;
   args.out_score = out_score;
   args.status = ctx->status;
   const int G = L.G;
   if (L.QT == 4)
-    return fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
-                               : run_score_k<4, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
-  return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(ctx, k, tq, tk, args, G, stream)
-                             : run_score_k<1, DSA_FMT_FP8>(ctx, k, tq, tk, args, G, stream);
+    return fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(ctx, ksel, tq, tk, args, G, stream)
+                               : run_score_k<4, DSA_FMT_FP8>(ctx, ksel, tq, tk, args, G, stream);
+  return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(ctx, ksel, tq, tk, args, G, stream)
+                             : run_score_k<1, DSA_FMT_FP8>(ctx, ksel, tq, tk, args, G, stream);
 }
 
 }  // namespace dsa

@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.dsa_index_topk_static.restype = ctypes.c_int
         L.dsa_get_device_status.argtypes = [_c_ptr, _c_ptr]
         L.dsa_get_device_status.restype = ctypes.c_int
+        L.dsa_ctx_set_slot_output.argtypes = [_c_ptr, _c_int]
+        L.dsa_ctx_set_slot_output.restype = ctypes.c_int
         L.dsa_ctx_set_hadamard.argtypes = [_c_ptr, _c_int]
         L.dsa_ctx_set_hadamard.restype = ctypes.c_int
         L.dsa_profile_enable.argtypes = [_c_ptr, ctypes.c_int]
@@ -204,6 +206,12 @@ class Context:
         st = lib().dsa_ctx_set_hadamard(self._h, 1 if on else 0)
         if st != 0:
             raise DsaError("dsa_ctx_set_hadamard", st)
+
+    def set_slot_output(self, on: bool = True):
+        """Top-k returns cache slots (page * 64 + offset) instead of positions."""
+        st = lib().dsa_ctx_set_slot_output(self._h, 1 if on else 0)
+        if st != 0:
+            raise DsaError("dsa_ctx_set_slot_output", st)
 
     def profile_enable(self, on: bool = True):
         st = lib().dsa_profile_enable(self._h, 1 if on else 0)

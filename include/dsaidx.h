@@ -127,6 +127,14 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
  * dsa_index_topk_workspace_size reports for bf16 caches. */
 dsa_status dsa_ctx_set_hadamard(dsa_ctx* ctx, int32_t on);
 
+/* Slot output: when on, dsa_index_topk writes into out_idx the cache slot of
+ * each selected key, page_table[b][pos / 64] * 64 + pos % 64 (the row the
+ * sparse attention gathers), instead of its position pos; padding stays -1.
+ * The pages feed the selected tokens to the attention ("The Crash That
+ * Changed Direction", section "The Experiment: Why fp32?"); the slot is what
+ * a paged gather needs. Off by default; applies to the calls made after it. */
+dsa_status dsa_ctx_set_slot_output(dsa_ctx* ctx, int32_t on);
+
 /* Upper bound of the workspace bytes dsa_index_topk needs for these sizes.
  * It does not grow with the context length: it holds the schedule
  * (O(Tq + B)), split-context partial lists (O(#SMs * k)) and, for fp8
@@ -153,7 +161,9 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  *              page are not read.
  *  seq_lens    (device) [B] int32, n_q(b) <= seq_lens[b] <= 64*max_pages.
  *  cu_q        (device) [B+1] int32, cu_q[0] = 0, non-decreasing, cu_q[B] = Tq.
- *  k           512 or 1024.  B <= 16384, Tq < 2^24 (else DSA_ERR_UNSUPPORTED).
+ *  k           1 .. 1024 (the pages use 512 and 1024; other k run the top-512
+ *              or top-1024 selection and keep the first k of each sorted
+ *              row).  B <= 16384, Tq < 2^24 (else DSA_ERR_UNSUPPORTED).
  *  out_idx     (device) [Tq][k] int32;  out_score (device) [Tq][k] fp32.
  *  workspace   (device) >= dsa_index_topk_workspace_size(...) bytes, 256-byte
  *              aligned; contents need not be initialised and are scratch.
