@@ -44,6 +44,22 @@ SCORER_SRC = os.path.join(ROOT, "dsa_sparse_attention_store_gb300", "csrc", "top
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def max_over_ranks(vals, device):
+    """Element-wise maximum over all ranks of a list of floats (the slowest
+    rank's times); one all_reduce on the process group's backend."""
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(v) for v in vals], device=device, dtype=torch.float64)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Units per second over the whole job: every rank does the same work per
+    step (weak scaling), timed by the slowest rank."""
+    return world * units_per_rank_step * steps / (ms / 1e3)
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -294,13 +310,12 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {st} after the timed steps")
 
     if dist:
-        t = torch.tensor([total_ms, e2e_ms or 0.0], device=dev, dtype=torch.float64)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+        total_ms, e2e_red = max_over_ranks([total_ms, e2e_ms or 0.0], dev)
+        e2e_ms = e2e_red if e2e_ms is not None else None
 
     ks_step = wl.key_scores() * len(fmts)
-    value = world * ks_step * args.steps / (total_ms / 1e3)
-    qps = world * wl.Tq * len(fmts) * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(ks_step, args.steps, world, total_ms)
+    qps = whole_job_rate(wl.Tq * len(fmts), args.steps, world, total_ms)
 
     # roofline of the scorer, per cache format (its launches in the timed region)
     peaks, peak_src = load_peaks()
@@ -355,7 +370,7 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if e2e_ms is not None:
-        out["e2e"] = {"value": world * ks_step * args.steps / (e2e_ms / 1e3), "unit": "key-scores/s",
+        out["e2e"] = {"value": whole_job_rate(ks_step, args.steps, world, e2e_ms), "unit": "key-scores/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "ms_per_step": e2e_ms / args.steps}
     ctx.close()
