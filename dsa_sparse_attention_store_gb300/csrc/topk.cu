@@ -26,7 +26,8 @@
 //   score   persistent, one CTA per SM, warp-specialised:
 //             warp 0      producer: page-table lookups, TMA of 64-token pages
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
-//                         x K=128 into one of two TMEM accumulators
+//                         x K=128 into a ring of TMEM accumulators (4 for
+//                         one-query tiles, 2 for four-query tiles)
 //             score warps tcgen05.ld, ReLU, head-weighted sum, fp8 key
 //                         scale, mask; one score per key staged in a ring of
 //                         shared-memory slots
@@ -394,7 +395,11 @@ struct Cfg {
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
   static constexpr int NWARPS = W_TOPK + 4 * NTK;
   static constexpr int NTHREADS = 32 * NWARPS;
-  static constexpr int TMEM_COLS = 2 * N;
+  // TMEM accumulator buffers: the MMA of a tile waits for the score warps
+  // to have read the buffer it reuses, so a deeper ring hides that round
+  // trip; four-query tiles fill the 512 columns with two
+  static constexpr int NTB = QT == 1 ? 4 : 2;
+  static constexpr int TMEM_COLS = NTB * N;
   static constexpr int Q_BYTES = N * 256;                 // bf16, or two e4m3 terms
   static constexpr int OP_BYTES = kTile * (FMT == DSA_FMT_BF16 ? 256 : 128);
   static constexpr int ST_BYTES = QT * kTile * 4;        // one staged tile of scores
@@ -414,7 +419,7 @@ struct Cfg {
 
 struct Misc {
   uint64_t op_full[8], op_empty[8];
-  uint64_t tm_full[2], tm_empty[2], q_full, q_empty, fin, w_full[2], w_empty[2];
+  uint64_t tm_full[4], tm_empty[4], q_full, q_empty, fin, w_full[2], w_empty[2];
   uint64_t st_full[16], st_empty[16];
   uint32_t tmem_base;
   int abort;
@@ -899,7 +904,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
       mbar_init(&ms->op_full[i], 1);
       mbar_init(&ms->op_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NTB; ++i) {
       mbar_init(&ms->tm_full[i], 1);
       mbar_init(&ms->tm_empty[i], C::NSW);
     }
@@ -1066,7 +1071,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         tc_fence_after();
         for (int t = s.t0; t < s.t1; ++t) {
           const int slot = tile_seq % C::S, u = tile_seq / C::S;
-          const int buf = tile_seq & 1, ub = tile_seq >> 1;
+          const int buf = tile_seq % C::NTB, ub = tile_seq / C::NTB;
           if (*abort_flag || !mbar_wait(&ms->op_full[slot], u & 1) ||
               !mbar_wait(&ms->tm_empty[buf], (ub & 1) ^ 1)) {
             if (!*abort_flag) atomicOr(a.status, DSA_DEV_TIMEOUT);
@@ -1157,7 +1162,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
         pid_n1 = pid_n2;
         pid_n2 = page_of(t + 2);
         scale_n1 = scale_of(pid_n1, t + 1);
-        const int buf = tile_seq & 1, ub = tile_seq >> 1;
+        const int buf = tile_seq % C::NTB, ub = tile_seq / C::NTB;
         const int sq = C::ALT ? rq : tile_seq;
         const int st = ring * C::RS + sq % C::RS, us = sq / C::RS;
         if (!__all_sync(0xffffffffu, mbar_wait(&ms->tm_full[buf], ub & 1))) {
