@@ -7,8 +7,23 @@
 #include <vector>
 
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace {
+
+// Self-test of the bounded waits: thread 0 waits on a shared-memory
+// mbarrier that nothing ever arrives at, with the scorer's wait and a budget
+// of `budget` clock cycles, then records DSA_DEV_TIMEOUT the way the scorer
+// does when a pipeline wait runs out, and the kernel returns.
+__global__ void bounded_wait_probe(unsigned int* status, long long budget) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    dsa::mbar_init(&bar, 1);
+    dsa::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !dsa::mbar_wait(&bar, 0, budget)) atomicOr(status, DSA_DEV_TIMEOUT);
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -162,6 +177,12 @@ dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms, int32_t* launches) {
   }
   ctx->prof_n = 0;
   return DSA_OK;
+}
+
+dsa_status dsa_selftest_bounded_wait(dsa_ctx* ctx, dsa_stream_t stream) {
+  if (!ctx) return DSA_ERR_INVALID_ARG;
+  bounded_wait_probe<<<1, 32, 0, as_stream(stream)>>>(ctx->status, 2000000LL);  // about 1 ms
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status dsa_get_device_status(dsa_ctx* ctx, dsa_stream_t stream) {

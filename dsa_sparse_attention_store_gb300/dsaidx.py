@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.dsa_index_topk_static.restype = ctypes.c_int
         L.dsa_get_device_status.argtypes = [_c_ptr, _c_ptr]
         L.dsa_get_device_status.restype = ctypes.c_int
+        L.dsa_selftest_bounded_wait.argtypes = [_c_ptr, _c_ptr]
+        L.dsa_selftest_bounded_wait.restype = ctypes.c_int
         L.dsa_ctx_set_slot_output.argtypes = [_c_ptr, _c_int]
         L.dsa_ctx_set_slot_output.restype = ctypes.c_int
         L.dsa_ctx_set_hadamard.argtypes = [_c_ptr, _c_int]
@@ -206,6 +208,12 @@ class Context:
         st = lib().dsa_ctx_set_hadamard(self._h, 1 if on else 0)
         if st != 0:
             raise DsaError("dsa_ctx_set_hadamard", st)
+
+    def selftest_bounded_wait(self, stream=None):
+        """Enqueue the bounded-wait self-test (records a timeout in the status)."""
+        st = lib().dsa_selftest_bounded_wait(self._h, _stream_ptr(stream))
+        if st != 0:
+            raise DsaError("dsa_selftest_bounded_wait", st)
 
     def set_slot_output(self, on: bool = True):
         """Top-k returns cache slots (page * 64 + offset) instead of positions."""

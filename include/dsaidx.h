@@ -222,6 +222,14 @@ dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms /* [DSA_K_COUNT] */,
  * word. Returns DSA_OK or the first device-side error recorded. */
 dsa_status dsa_get_device_status(dsa_ctx* ctx, dsa_stream_t stream);
 
+/* Failure-detection self-test: enqueues a one-CTA kernel that waits, with
+ * the scorer's bounded mbarrier wait, on a barrier nothing ever signals;
+ * after about a millisecond the wait gives up, DSA_ERR_TIMEOUT is recorded
+ * in the status word (read it with dsa_get_device_status) and the kernel
+ * returns, leaving the context usable. Exercises the error path of a stalled
+ * pipeline without faulting or hanging the GPU. */
+dsa_status dsa_selftest_bounded_wait(dsa_ctx* ctx, dsa_stream_t stream);
+
 /* Static string for a status code. */
 const char* dsa_status_str(dsa_status s);
 

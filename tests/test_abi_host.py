@@ -78,6 +78,7 @@ def test_invalid_arguments_rejected_without_device(L):
     # settings on a null context
     assert L.dsa_ctx_set_hadamard(None, 1) == 1
     assert L.dsa_ctx_set_slot_output(None, 1) == 1
+    assert L.dsa_selftest_bounded_wait(None, None) == 1
     # k outside 1 .. 1024
     assert L.dsa_index_topk(fake, *args, 0, good, good, good, 1 << 30, None) == 2
     assert L.dsa_index_topk(fake, *args, 1025, good, good, good, 1 << 30, None) == 2
