@@ -85,10 +85,17 @@ def load_peaks():
 
 
 def scorer_hash() -> str:
+    """Hash of the scorer's code (comments and blank space removed, so that
+    a comment edit does not invalidate a traffic capture; any code change
+    does)."""
+    import re
     h = hashlib.sha256()
     for name in ("topk.cu", "ptx.cuh", "internal.cuh"):
-        with open(os.path.join(os.path.dirname(SCORER_SRC), name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(os.path.dirname(SCORER_SRC), name), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,24 +5,26 @@
 // 64 index heads are multiplied against all cached index keys (a batched
 // matrix product), each head's dot product goes through a ReLU, the heads are
 // combined with per-head weights into one score per key, keys after the
-// query's position are masked, and the top-k positions (k = 512 or 1024) are
-// kept. Fp8 keys enter the product as stored (e4m3 tensor-core operands).
+// query's position are masked, and the top-k positions are kept (k = 512 or
+// 1024 on the pages; any k up to 1024 here). Fp8 keys enter the product as
+// stored (e4m3 tensor-core operands).
 //
 // Why it streams ("When the Fused Kernel Isn't Enough", section "The
 // Message: Validation and Discovery"): materialising the [q_len x ctx]
 // logits ran out of memory at 22K tokens. Here every score lives only in
 // registers; key tiles stream through a per-query running top-k in shared
 // memory. Scratch is the schedule, at most two partial top-k lists per CTA
-// (when a query tile's context is split across CTAs) and, for fp8 caches,
-// the queries converted for the tensor cores.
+// (when a query tile's context is split across CTAs) and, for fp8 caches or
+// with the Hadamard rotation, the prepared queries.
 //
 // Kernels, in launch order (all with programmatic dependent launch):
 //   plan    one CTA: query tiles (QT queries of one sequence), a prefix sum
 //           of their key-tile counts, and each CTA's first query tile, so the
 //           CTAs split the total work evenly with one dependent load.
-//   qprep   fp8 caches only: q -> two e4m3 terms with a power-of-two scale
-//           per (query, head), the scale's inverse folded into the head
-//           weight, so the tensor cores take the stored e4m3 keys as they are.
+//   qprep   fp8 caches or Hadamard rotation only: q rotated (if on) and, for
+//           fp8 caches, split into two e4m3 terms with a power-of-two scale
+//           per (query, head), the scales folded into the head weights, so
+//           the tensor cores take the stored e4m3 keys as they are.
 //   score   persistent, one CTA per SM, warp-specialised:
 //             warp 0      producer: page-table lookups, TMA of 64-token pages
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
@@ -32,11 +34,14 @@
 //                         scale, mask; one score per key staged in a ring of
 //                         shared-memory slots
 //             top-k groups of 4 warps: threshold filter of the staged scores
-//                         into a running top-k per query, compacted by radix
-//                         select when full; at the end of a query tile exact
-//                         selection, sort and output (or, for a query tile
-//                         split across CTAs, a sorted partial list, merged by
-//                         the piece that finishes last)
+//                         into a running top-k per query (one-query tiles:
+//                         two groups on alternate query tiles, each merging
+//                         candidate batches into a sorted list; four-query
+//                         tiles: one group per query, a buffer cut back by
+//                         radix select and sorted at the end); then output
+//                         (or, for a query tile split across CTAs, a sorted
+//                         partial list, merged by the piece that finishes
+//                         last)
 //           Keys sit on the MMA's M dimension so each score thread owns one
 //           key (one TMEM lane) and reduces over heads in its own registers.
 #include <cuda_bf16.h>
@@ -57,8 +62,8 @@ constexpr int kTile = 128;  // keys per MMA tile = 2 pages
 constexpr int kPageBytesFp8 = 64 * 128 + 64 * 4;
 
 // The work is split evenly in units: a query tile with n key tiles costs
-// n + ovh units, ovh standing for its fixed costs (query load, final
-// selection and sort), so CTAs that get many short query tiles get fewer.
+// n + ovh units, ovh standing for its fixed costs (query load, final merge
+// or selection and sort), so CTAs that get many short query tiles get fewer.
 struct PlanHdr {
   int qtot;         // query tiles
   int Ge;           // CTAs with work: min(grid, total units)
@@ -437,7 +442,7 @@ struct ScoreArgs {
   int causal;
   const uint8_t* cache;
   int num_pages;
-  const float* w;  // head weights (fp8: with the query scale folded in)
+  const float* w;  // head weights (prepared queries: with their scales folded in)
   long long qrows;  // (query, head) rows; fp8: the second e4m3 term's rows follow
   const char* ws;
   WsLayout L;
