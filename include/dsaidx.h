@@ -15,9 +15,10 @@
  *        page and an offset and its 128 values are written there.
  *  [CRA] "The Crash That Changed Direction", sections "The Experiment: Why
  *        fp32?" and "Assumptions Made and Broken": scores come from a batched
- *        matrix product of queries and index keys followed by a ReLU; fp8
- *        keys are up-converted exactly before the product; the top-512 (or
- *        1024) key positions are kept.
+ *        matrix product of queries and index keys followed by a ReLU; the
+ *        pages up-convert fp8 keys exactly before the product (this library
+ *        gives them to the tensor cores as stored, see dsa_index_topk); the
+ *        top-512 (or 1024) key positions are kept.
  *  [WFK] "When the Fused Kernel Isn't Enough", section "The Message:
  *        Validation and Discovery": materialising the logits over the whole
  *        context ran out of memory at about 22K tokens. This library never
@@ -52,7 +53,7 @@ typedef struct CUstream_st* dsa_stream_t; /* a cudaStream_t; NULL = legacy defau
 typedef enum {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer ... */
-  DSA_ERR_UNSUPPORTED = 2,   /* k not in {512, 1024}, unknown format, no sm_103 device */
+  DSA_ERR_UNSUPPORTED = 2,   /* k not in 1..1024, unknown format, no sm_103 device */
   DSA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
   DSA_ERR_DEVICE_BOUNDS = 4, /* device saw a page id / position / sequence out of range */
   DSA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
@@ -138,7 +139,7 @@ dsa_status dsa_ctx_set_slot_output(dsa_ctx* ctx, int32_t on);
 /* Upper bound of the workspace bytes dsa_index_topk needs for these sizes.
  * It does not grow with the context length: it holds the schedule
  * (O(Tq + B)), split-context partial lists (O(#SMs * k)) and, for fp8
- * caches, the queries converted for the tensor cores (O(Tq)). */
+ * caches or with the Hadamard rotation on, the prepared queries (O(Tq)). */
 size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k,
                                      dsa_fmt fmt);
 
@@ -177,7 +178,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
 
 /* Allocation-free top-k, for callers that cannot allocate device memory
  * (an engine whose memory is already carved into its own pools, or a
- * latency-critical path that must not call cudaMalloc). The paper has no
+ * latency-critical path that must not call cudaMalloc). The pages have no
  * counterpart; it is an addition of this library.
  * Same arguments and results as dsa_index_topk, without the workspace: the
  * scratch is a fixed array of DSA_STATIC_WORKSPACE_BYTES in the library's
@@ -189,9 +190,10 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
  * zero. Returns DSA_ERR_WORKSPACE, without launching anything, when
  * dsa_index_topk_workspace_size(ctx, Tq, B, k, fmt) exceeds
  * DSA_STATIC_WORKSPACE_BYTES (on a 152-SM GB300 with one sequence: bf16
- * batches up to about 2.9M queries; fp8 batches up to 1417 queries with
- * k = 1024 and 1716 with k = 512, since fp8 caches keep the converted
- * queries, 16.6 KB each, in the scratch). */
+ * batches up to about 2.0M queries with k <= 512 and 1.7M with k > 512;
+ * fp8 batches, and bf16 batches with the Hadamard rotation on, up to about
+ * 1700 and 1400 queries, since they keep the prepared queries, 16.6 KB
+ * each, in the scratch). */
 #define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
 dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_w,
                                  const void* cache, int32_t num_pages, dsa_fmt fmt,
