@@ -3,8 +3,12 @@
 This module is shared by the tests, the bench and the oracle harness. It
 draws random numbers and lays them out in the shapes the indexer consumes;
 it holds none of the indexer's own arithmetic (no normalisation, no
-rotation, no quantisation, no scoring). Everything is counter-based, so the
-same (seed, stream, index) gives the same value on any machine.
+quantisation, no scoring, and neither side calls it to compute a result).
+The one rotation here is the needle workload's: to plant a key that points
+along a chosen direction after the store, the raw row is that direction
+turned back by its RoPE angle (an input construction in float64).
+Everything is counter-based, so the same (seed, stream, index) gives the
+same value on any machine.
 
 Generator: SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom
 number generators", OOPSLA 2014): state_i = base + (i + 1) * 0x9E3779B97F4A7C15,
