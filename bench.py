@@ -60,6 +60,20 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms: float
     return world * units_per_rank_step * steps / (ms / 1e3)
 
 
+def scorer_algorithmic(wl, fmt: int):
+    """(bytes, flops) one scorer launch must move / do for workload wl in
+    cache format fmt: every visible key read once (256 B bf16, 132 B fp8),
+    the queries (16 KB each, bf16 or two e4m3 terms) and head weights, one
+    4-byte page id per page, 8 bytes per output entry; 2 * 64 * 128 flops
+    per (query, visible key) pair."""
+    import numpy as np
+    pages = sum((int(L) + 63) // 64 for L in wl.seq_lens)
+    nbytes = (int(wl.seq_lens.astype(np.int64).sum()) * TOKEN_BYTES[fmt]
+              + wl.Tq * 64 * 128 * 2 + wl.Tq * 64 * 4
+              + pages * 4 + wl.Tq * wl.k * 8)
+    return nbytes, wl.key_scores() * 2 * 64 * 128
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -327,15 +341,10 @@ def run_ours(args, rank, world, local_rank):
     # roofline of the scorer, per cache format (its launches in the timed region)
     peaks, peak_src = load_peaks()
     launches_per_step = launches / max(args.steps, 1)
-    pages = sum((int(L) + 63) // 64 for L in wl.seq_lens)
-    flops_launch = wl.key_scores() * 2 * 64 * 128
-
     def roofline(f):
         sc_ms, sc_n = prof["score_" + FMT_NAMES[f]]
         avg_ms = sc_ms / max(sc_n, 1)
-        nbytes = (int(wl.seq_lens.astype(np.int64).sum()) * TOKEN_BYTES[f]   # keys, read once
-                  + wl.Tq * 64 * 128 * 2 + wl.Tq * 64 * 4                        # q, head_w
-                  + pages * 4 + wl.Tq * wl.k * 8)                                # page ids, top-k out
+        nbytes, flops_launch = scorer_algorithmic(wl, f)
         hbm = nbytes / (avg_ms / 1e3) / 1e9
         tc = flops_launch / (avg_ms / 1e3) / 1e12
         traffic = None
