@@ -23,7 +23,8 @@ E4M3_MAX = 448.0
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact value of bf16 bit patterns."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN patterns widen to NaN
+        return b.view(np.float32).astype(np.float64)
 
 
 def f32_to_bf16(x: np.ndarray) -> np.ndarray:
