@@ -120,6 +120,10 @@ dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_
 
 dsa_status dsa_ctx_destroy(dsa_ctx* ctx) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
+  // free on the context's device, whichever device is current, and restore it
+  int cur = -1;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  if (have_cur && cur != ctx->device) cudaSetDevice(ctx->device);
   cudaDeviceSynchronize();
   cudaFree(ctx->rope);
   cudaFree(ctx->gamma);
@@ -132,6 +136,7 @@ dsa_status dsa_ctx_destroy(dsa_ctx* ctx) {
     delete[] ctx->prof;
   }
   delete ctx;
+  if (have_cur && cur >= 0) cudaSetDevice(cur);
   return DSA_OK;
 }
 
@@ -164,6 +169,7 @@ dsa_status dsa_profile_enable(dsa_ctx* ctx, int on) {
 
 dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms, int32_t* launches) {
   if (!ctx || !ms || !launches) return DSA_ERR_INVALID_ARG;
+  if (const dsa_status d = dsa::check_device(ctx)) return d;
   for (int k = 0; k < DSA_K_COUNT; ++k) {
     ms[k] = 0.f;
     launches[k] = static_cast<int32_t>(ctx->launches[k]);
@@ -181,12 +187,14 @@ dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms, int32_t* launches) {
 
 dsa_status dsa_selftest_bounded_wait(dsa_ctx* ctx, dsa_stream_t stream) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
+  if (const dsa_status d = dsa::check_device(ctx)) return d;
   bounded_wait_probe<<<1, 32, 0, as_stream(stream)>>>(ctx->status, 2000000LL);  // about 1 ms
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status dsa_get_device_status(dsa_ctx* ctx, dsa_stream_t stream) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
+  if (const dsa_status d = dsa::check_device(ctx)) return d;
   unsigned int w = 0;
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DSA_ERR_CUDA;
   if (cudaMemcpy(&w, ctx->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess ||
@@ -209,6 +217,7 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
   if (!aligned(k_raw, 16) || !aligned(cache, 256) || !aligned(rope_pos, 4) || !aligned(seq_id, 4) ||
       !aligned(page_table, 4))
     return DSA_ERR_INVALID_ARG;
+  if (const dsa_status d = dsa::check_device(ctx)) return d;
   return dsa::launch_store(ctx, k_raw, rope_pos, seq_id, page_table, T, B, max_pages, cache,
                            num_pages, fmt, as_stream(stream));
 }
@@ -239,6 +248,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
   if (!aligned(q, 16) || !aligned(cache, 256) || !aligned(workspace, 256) || !aligned(head_w, 16) ||
       !aligned(out_idx, 4) || !aligned(out_score, 4))
     return DSA_ERR_INVALID_ARG;
+  if (const dsa_status d = dsa::check_device(ctx)) return d;
   if (ws_bytes < dsa::topk_workspace(ctx, Tq, B, k, fmt)) return DSA_ERR_WORKSPACE;
   return dsa::launch_topk(ctx, q, head_w, cache, num_pages, fmt, page_table, max_pages, seq_lens,
                           cu_q, B, Tq, causal ? 1 : 0, k, out_idx, out_score, workspace, ws_bytes,

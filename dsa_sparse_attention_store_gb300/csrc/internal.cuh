@@ -38,6 +38,17 @@ struct dsa_ctx {
 
 namespace dsa {
 constexpr int kProfCap = 8192;
+
+// Every call that enqueues work first checks that the calling thread's
+// current device is the context's: the kernels launch on the current device
+// but read the context's device memory (table, gamma, status word), so a
+// call made with another device current is rejected before anything is
+// enqueued. Returns DSA_ERR_CUDA when no device can be queried.
+inline dsa_status check_device(const dsa_ctx* ctx) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  return dev == ctx->device ? DSA_OK : DSA_ERR_INVALID_ARG;
+}
 // Record the start/end of one kernel launch of kind `kind` on `stream`.
 struct LaunchScope {
   dsa_ctx* ctx;

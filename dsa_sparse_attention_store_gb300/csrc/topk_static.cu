@@ -14,7 +14,9 @@
 // every GPU that loads the library holds it until the process exits. Host
 // code cannot use the array's name as a device address, so the address is
 // looked up with cudaGetSymbolAddress once per device, on the first call made
-// with that device current (make that first call before any stream capture).
+// with that device current (make that first call before any stream capture),
+// and again if the device's CUDA context has changed since (after a device
+// reset the module is loaded anew and the array may have moved).
 // All calls share the array and it keeps the last call's contents: calls that
 // overlap on the GPU (different streams, or different threads without
 // ordering) race on it. Nothing in it needs clearing between calls: the
@@ -32,17 +34,41 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_ptr[kMaxDevices] = {};
+CUcontext g_owner[kMaxDevices] = {};  // the CUDA context the cached address belongs to
 
-// Device address of the scratch array for the current device (looked up once).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The calling thread's current CUDA context (null if it cannot be read).
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of the scratch array for the current device. Looked up
+// once per device and CUDA context: after a device reset the runtime loads
+// the module again in a new context, where the array may sit elsewhere, so a
+// changed context triggers a new lookup.
 dsa_status static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
+  const CUcontext cur = current_context();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ptr[dev]) {
+  if (!g_ptr[dev] || !cur || g_owner[dev] != cur) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dsa_static_ws) != cudaSuccess || !p) return DSA_ERR_CUDA;
     g_ptr[dev] = p;
+    g_owner[dev] = current_context();  // the lookup made the device's context current
   }
   *out = g_ptr[dev];
   return DSA_OK;
@@ -71,6 +97,7 @@ extern "C" dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const f
   if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(cache) & 255) ||
       (reinterpret_cast<uintptr_t>(head_w) & 15) || !aligned4(out_idx) || !aligned4(out_score))
     return DSA_ERR_INVALID_ARG;
+  if (const dsa_status d = dsa::check_device(ctx)) return d;
   // the sizes must fit the fixed scratch array; nothing is allocated instead
   if (dsa::topk_workspace(ctx, Tq, B, k, fmt) > static_cast<size_t>(DSA_STATIC_WORKSPACE_BYTES))
     return DSA_ERR_WORKSPACE;

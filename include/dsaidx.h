@@ -30,7 +30,10 @@
  *    pointers marked (host) are host memory. The library keeps no pointer
  *    after a call returns.
  *  - Work is enqueued on `stream` and is asynchronous; argument errors are
- *    returned before anything is enqueued. A launch failure returns
+ *    returned before anything is enqueued. Calls that enqueue work must be
+ *    made with the context's device current (the one current at
+ *    dsa_ctx_create); otherwise they return DSA_ERR_INVALID_ARG and enqueue
+ *    nothing. A launch failure returns
  *    DSA_ERR_CUDA. Errors found on the device (a page id out of range, a
  *    bounded wait that ran out) do not trap: the kernel skips the access,
  *    records the error in a status word of the context and carries on;
@@ -185,7 +188,9 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
  * device image, held by every GPU that loads the library until exit. The
  * call allocates nothing. Its first call on a device looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture. All calls share the array: calls that overlap on the GPU
+ * stream capture. A device reset (cudaDeviceReset) invalidates that address:
+ * the next call notices the new CUDA context and looks it up again, so make
+ * it, too, outside a capture. All calls share the array: calls that overlap on the GPU
  * race. Nothing in it needs clearing; each call rewrites what must start at
  * zero. Returns DSA_ERR_WORKSPACE, without launching anything, when
  * dsa_index_topk_workspace_size(ctx, Tq, B, k, fmt) exceeds

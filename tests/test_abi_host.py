@@ -93,3 +93,22 @@ def test_context_creation_without_gpu_fails_cleanly(L):
     st = L.dsa_ctx_create(ctypes.byref(h), ctypes.c_float(10000.0), ctypes.c_float(1e-6), 64, None)
     assert st in (2, 3) and not h.value
     assert L.dsa_ctx_create(ctypes.byref(h), ctypes.c_float(-1.0), ctypes.c_float(1e-6), 64, None) == 1
+
+
+def test_device_is_checked_before_the_context_is_read(L):
+    # With every argument valid, the next step is the check that the current
+    # device is the context's. Without a GPU it cannot pass (no device to
+    # query), so the call returns DSA_ERR_CUDA before the fake context below
+    # is ever dereferenced or anything is enqueued.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU (the context pointer is fake)")
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    good = P(0x100000)
+    assert L.dsa_index_store(fake, good, good, good, good, 1, 1, 1, good, 1, 0, None) == 3
+    args = [good, good, good, 1, 0, good, 1, good, good, 1, 4, 1]
+    assert L.dsa_index_topk(fake, *args, 512, good, good, good, 1 << 30, None) == 3
+    assert L.dsa_index_topk_static(fake, *args, 512, good, good, None) == 3
+    assert L.dsa_get_device_status(fake, None) == 3
+    assert L.dsa_selftest_bounded_wait(fake, None) == 3

@@ -1,7 +1,10 @@
 """Failure detection on the GPU without a GPU fault: a bounded wait that runs
-out is reported through the status word and leaves the context usable, a
-corrupt page table is reported and skipped, and no call writes outside its
-output, workspace or cache buffers (canary bytes around each)."""
+out is reported through the status word and leaves the context usable; an
+out-of-range page id in the page table the scorer reads is reported and its
+page skipped (the store's own check is in test_gpu_store.py); a call made
+with another device current is refused before anything is enqueued; and no
+call writes outside its output, workspace or cache buffers (canary bytes
+around each)."""
 import numpy as np
 import pytest
 
@@ -101,4 +104,69 @@ def test_no_writes_outside_buffers(ctx, fmt, shape):
     rows = np.arange(wl.Tq) if wl.Tq <= 200 else np.linspace(0, wl.Tq - 1, 200).astype(np.int64)
     o_i, o_s, full = U.oracle_topk(wl, fmt, ocache, rows)
     ok, reps = P.compare(rows, oi.cpu().numpy()[rows], os_.cpu().numpy()[rows], o_i, o_s, full, k, fmt)
+    assert ok, P.summary(reps)
+
+
+def test_wrong_device_rejected_without_launch():
+    # a context made on device 0, called with device 1 current: the call must
+    # be refused before anything is enqueued (the kernels would run on device
+    # 1 but read device 0's table and status word)
+    import torch
+    from dsa_sparse_attention_store_gb300 import Context, dsaidx
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two GPUs")
+    torch.cuda.set_device(0)
+    c = Context(theta=10000.0, eps=1e-6, max_pos=4096)
+    try:
+        wl = I.make_workload("wd", [300], [2], [300], True, 512, seed=54, wid=54)
+        torch.cuda.set_device(1)
+        d = U.device_workload(wl, S.FMT_BF16, c, store_fill=False, store_new=False)
+        k = U.t_bf16(wl.new_k).cuda()
+        pos = torch.from_numpy(wl.new_pos).cuda()
+        seq = torch.from_numpy(wl.new_seq).cuda()
+        with pytest.raises(dsaidx.DsaError) as e:
+            c.store(k, pos, seq, d["page_table"], d["cache"], wl.num_pages, S.FMT_BF16)
+        assert e.value.status == 1
+        torch.cuda.synchronize()
+        assert int(d["cache"].sum()) == 0
+    finally:
+        torch.cuda.set_device(0)
+        c.close()
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("shape", ["decode", "prefill"])
+def test_scorer_skips_out_of_range_page(ctx, fmt, shape):
+    # the keys are stored through a valid page table; top-k then reads a copy
+    # in which one page id of sequence 0 (positions 192..255) points past the
+    # cache. The scorer skips that page (no copy is issued for it, its keys
+    # score -inf), records DSA_ERR_DEVICE_BOUNDS and carries on; rows that
+    # never see positions 192..255 must still match the oracle.
+    import torch
+    if shape == "decode":
+        wl = I.make_workload("bd", [3000, 900, 5000], [1, 1, 1], [1, 1, 1], True, 512, seed=55, wid=55)
+        rows = np.array([1, 2])                      # sequence 0's query sees the bad page
+    else:
+        wl = I.make_workload("bf", [700, 300], [700, 300], [700, 300], True, 512, seed=56, wid=56)
+        rows = np.concatenate([np.arange(0, 192), np.arange(700, 1000)])
+    d = U.device_workload(wl, fmt, ctx)
+    assert ctx.device_status() == 0
+    bad_pt = d["page_table"].clone()
+    bad_pt[0, 3] = wl.num_pages + 7
+    k = wl.k
+    oi = torch.empty((wl.Tq, k), dtype=torch.int32, device="cuda")
+    os_ = torch.empty((wl.Tq, k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ctx.topk_workspace_size(wl.Tq, wl.B, k, fmt), dtype=torch.uint8, device="cuda")
+    ctx.topk(d["q"], d["head_w"], d["cache"], wl.num_pages, fmt, bad_pt, d["seq_lens"], d["cu_q"],
+             wl.causal, k, oi, os_, ws)
+    assert ctx.device_status() == 4                   # DSA_ERR_DEVICE_BOUNDS, no trap
+    assert ctx.device_status() == 0                   # read and cleared
+    gi, gs = oi.cpu().numpy(), os_.cpu().numpy()
+    # no row selects a position of the skipped page
+    b = np.searchsorted(wl.cu_q, np.arange(wl.Tq), side="right") - 1
+    in_bad = (b[:, None] == 0) & (gi >= 192) & (gi < 256)
+    assert not in_bad.any()
+    cache = U.oracle_cache(wl, fmt)
+    o_i, o_s, full = U.oracle_topk(wl, fmt, cache, rows)
+    ok, reps = P.compare(rows, gi[rows], gs[rows], o_i, o_s, full, k, fmt)
     assert ok, P.summary(reps)

@@ -2,7 +2,8 @@
 cannot allocate device memory (an engine that has already split all free
 memory into its own pools, or a latency-critical path where cudaMalloc is not
 allowed). It must give the same results as dsa_index_topk with a caller
-workspace, on two calls in a row that share its fixed scratch array, and
+workspace and pass the oracle comparison, on two calls in a row that share
+its fixed scratch array, leave the device's free memory unchanged, and
 reject sizes beyond that array without launching.
 
 This file is collected last so that a run stopping at the first failure has
@@ -15,6 +16,7 @@ import pytest
 
 from synth import inputs as I
 from tests import gpu_util as U
+from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
@@ -45,19 +47,36 @@ def test_static_scratch_matches_workspace_path(fmt):
                                                 seed=42, wid=41)]):
             d = U.device_workload(wl, fmt, ctx)
             ref_i, ref_s = U.run_topk(wl, fmt, ctx, d)
+            outs = [(torch.full((wl.Tq, wl.k), 7, dtype=torch.int32, device="cuda"),
+                     torch.full((wl.Tq, wl.k), 7.0, dtype=torch.float32, device="cuda")) for _ in range(2)]
+            # a first call looks up the scratch array (it may load the module);
+            # after it, the calls must not change the device's free memory
+            assert _call_static(ctx, wl, fmt, d, wl.k, *outs[0]) == 0
+            torch.cuda.synchronize()
+            free0 = torch.cuda.mem_get_info()[0]
             for call in range(2):   # two calls in a row share the static scratch
-                out_i = torch.full((wl.Tq, wl.k), 7, dtype=torch.int32, device="cuda")
-                out_s = torch.full((wl.Tq, wl.k), 7.0, dtype=torch.float32, device="cuda")
+                out_i, out_s = outs[call]
+                out_i.fill_(7)
+                out_s.fill_(7.0)
                 st = _call_static(ctx, wl, fmt, d, wl.k, out_i, out_s)
                 assert st == 0, f"workload {n} call {call}: status {st}"
-                torch.cuda.synchronize()
-                assert ctx.device_status() == 0
-                gi, gs = out_i.cpu().numpy(), out_s.cpu().numpy()
-                # same kernels and inputs: positions equal, scores within the bf16 logit tolerance
+            torch.cuda.synchronize()
+            assert torch.cuda.mem_get_info()[0] == free0, "the static entry point allocated device memory"
+            assert ctx.device_status() == 0
+            cache = U.oracle_cache(wl, fmt)
+            rows = np.arange(wl.Tq)
+            o_i, o_s, full = U.oracle_topk(wl, fmt, cache, rows)
+            for call in range(2):
+                gi, gs = outs[call][0].cpu().numpy(), outs[call][1].cpu().numpy()
+                # same kernels and inputs as the workspace path: positions equal,
+                # scores within the bf16 logit tolerance of its scores
                 assert np.array_equal(gi, ref_i), f"workload {n} call {call}: positions differ"
                 fin = np.isfinite(ref_s)
                 assert np.array_equal(fin, np.isfinite(gs))
                 assert np.allclose(gs[fin], ref_s[fin], rtol=2e-3, atol=0)
+                # and against the oracle, with the rules every other top-k test uses
+                ok, reps = P.compare(rows, gi, gs, o_i, o_s, full, wl.k, fmt)
+                assert ok, P.summary(reps)
     finally:
         ctx.close()
 
