@@ -20,10 +20,13 @@ on those float64 values. Top-k = the first min(k, visible) keys in the order
 are reported rounded to fp32.
 
 With a Hadamard-rotated cache (see oracle.store) the stored key is H k; each
-query head is rotated by the same fp32 butterflies and rounded to bf16 (the
-rotated query is a bf16 operand, like the plain one), and the dot products
-are divided by 128 (exact), so the scores are those of the unrotated vectors
-up to the store's and the query's rounding.
+query head is rotated by the same matrix H, exactly (a float64 product with
+the +-1 Sylvester matrix: sums of 128 bf16 values), and the dot products are
+divided by 128 (exact). The pages require only that queries and keys use the
+same order ("The Fused Kernel Decision", section "Assumptions and Their
+Validity"); they round nothing on the query side, so the rotated query is
+not rounded here either and (H q) . (H k) / 128 = q . k holds up to the
+store's rounding of k.
 """
 from __future__ import annotations
 
@@ -64,8 +67,7 @@ def scores(keys: np.ndarray, q_bits: np.ndarray, w: np.ndarray, hadamard: bool =
     m = q_bits.shape[0]
     qf = F.bf16_to_f64(q_bits).reshape(m * H, S.D)
     if hadamard:
-        qr = S.wht_f32(qf.astype(np.float32))              # exact input: bf16 -> fp32
-        qf = F.bf16_to_f64(F.f32_to_bf16(qr)) / 128.0
+        qf = (qf @ sylvester().T) / 128.0
     dots = keys @ qf.T                                   # [n, m*64]
     dots = np.maximum(dots, 0.0).reshape(keys.shape[0], m, H)
     return np.einsum("nmh,mh->mn", dots, np.asarray(w, dtype=np.float64))

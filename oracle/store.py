@@ -81,8 +81,10 @@ def rope_cos_sin(theta: float, positions: np.ndarray):
     return cu[inv], su[inv]
 
 
-def rmsnorm_f32(x: np.ndarray, eps: float, gamma: np.ndarray | None = None) -> np.ndarray:
-    """RMSNorm of fp32 rows [T,128] in the fixed fp32 order stated above."""
+def sum_squares_f32(x: np.ndarray) -> np.ndarray:
+    """fp32 sum of squares of rows [T,128] in the fixed order stated above:
+    16 partials over dims 8g..8g+7 in dim order, then pairwise (g, g+8),
+    (g, g+4), (g, g+2), (g, g+1)."""
     x = np.asarray(x, dtype=np.float32)
     T = x.shape[0]
     sq = (x * x).reshape(T, 16, 8)            # exact: x has <= 8 significant bits
@@ -92,7 +94,13 @@ def rmsnorm_f32(x: np.ndarray, eps: float, gamma: np.ndarray | None = None) -> n
     t = p[:, :8] + p[:, 8:]
     t = t[:, :4] + t[:, 4:]
     t = t[:, :2] + t[:, 2:]
-    ss = t[:, 0] + t[:, 1]
+    return t[:, 0] + t[:, 1]
+
+
+def rmsnorm_f32(x: np.ndarray, eps: float, gamma: np.ndarray | None = None) -> np.ndarray:
+    """RMSNorm of fp32 rows [T,128] in the fixed fp32 order stated above."""
+    x = np.asarray(x, dtype=np.float32)
+    ss = sum_squares_f32(x)
     ms = ss * np.float32(1.0 / 128.0)
     r = np.float32(1.0) / np.sqrt(ms + np.float32(eps))
     y = x * r[:, None]

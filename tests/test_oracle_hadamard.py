@@ -95,13 +95,13 @@ def test_bruteforce_tiny_rotated():
     oi, os_ = X.index_topk(cache, S.FMT_BF16, wl.page_table, wl.seq_lens, wl.cu_q, wl.q,
                            wl.head_w, True, 8, hadamard=True)
     keys = S.read_keys(cache, S.FMT_BF16, wl.page_table[0], 90).tolist()
+    Hm = X.sylvester().tolist()
     for r in range(wl.Tq):
         qpos = 90 - 3 + r
         qv = F.bf16_to_f64(wl.q[r]).tolist()
         w = [float(v) for v in wl.head_w[r]]
-        # the query heads rotated (fp32 butterflies, pinned above) and rounded
-        # to bf16, the rotated query's precision
-        qr = F.bf16_to_f64(F.f32_to_bf16(S.wht_f32(np.asarray(qv, dtype=np.float32)))).tolist()
+        # the query heads rotated by the explicit matrix, one head at a time
+        qr = [[sum(Hm[i][j] * qv[h][j] for j in range(128)) for i in range(128)] for h in range(64)]
         sc = []
         for p in range(qpos + 1):
             tot = 0.0
@@ -114,3 +114,20 @@ def test_bruteforce_tiny_rotated():
         order = sorted(range(qpos + 1), key=lambda i: (-sc[i], i))[:8]
         assert [int(v) for v in oi[r] if v >= 0] == order
         assert np.allclose(os_[r, :8], [sc[i] for i in order], rtol=1e-6, atol=1e-6)
+
+
+def test_rotated_scores_equal_plain_scores_on_exact_keys():
+    # keys that are exactly H v (small integers v: every entry of H v is an
+    # integer below 2^11, exact in float64): with the query rotated exactly,
+    # (H q) . (H v) / 128 = q . v, so the rotated scores equal the plain
+    # scores of v to float64 rounding. A query rotation rounded to bf16 (8
+    # significant bits) would miss by about 1e-3 of the scores.
+    rng = np.random.default_rng(9)
+    v = rng.integers(-4, 5, (40, 128)).astype(np.float64)
+    keys_rot = v @ X.sylvester().T
+    q_bits = I.to_bf16_bits(rng.standard_normal((5, 64, 128)).astype(np.float32))
+    w = (rng.standard_normal((5, 64)) / 8).astype(np.float32)
+    plain = X.scores(v, q_bits, w)
+    rot = X.scores(keys_rot, q_bits, w, hadamard=True)
+    scale = np.abs(plain).max(axis=1, keepdims=True)
+    assert np.all(np.abs(rot - plain) <= 1e-12 * scale)

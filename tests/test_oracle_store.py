@@ -51,6 +51,39 @@ def test_rmsnorm_one_hot(j, a):
         assert abs(abs(y[0, j]) - math.sqrt(128)) < 1e-3 * math.sqrt(128)
 
 
+def _rms_order_golden():
+    dims, bits = {}, {}
+    for ln in open(os.path.join(GOLD, "rmsnorm_order.txt")):
+        ln = ln.split("#")[0].split()
+        if len(ln) != 2:
+            continue
+        if ln[0].isdigit():
+            dims[int(ln[0])] = float(ln[1])
+        else:
+            bits[ln[0]] = int(ln[1], 16)
+    return dims, bits
+
+
+def test_rmsnorm_sum_of_squares_order_golden():
+    # a key whose fp32 sum of squares depends on the order of the additions;
+    # the expected bits are derived by hand in the golden file
+    dims, bits = _rms_order_golden()
+    x = np.zeros((1, 128), np.float32)
+    for d, v in dims.items():
+        x[0, d] = v
+    assert np.array_equal(F.bf16_to_f64(_bf16(x)), x.astype(np.float64))   # exact in bf16
+    ss = S.sum_squares_f32(x)
+    assert int(ss.view(np.uint32)[0]) == bits["ss"]
+    # the golden tells the defined order from the orders a mistake could take
+    others = {k: v for k, v in bits.items() if k != "ss"}
+    assert len(others) >= 4 and bits["ss"] not in others.values()
+    # and the whole norm uses that sum: y = x * (1 / sqrt(ss / 128 + eps))
+    y = S.rmsnorm_f32(x, 1e-6)
+    ssv = float(np.uint32(bits["ss"]).view(np.float32))
+    r = 1.0 / math.sqrt(ssv / 128.0 + float(np.float32(1e-6)))
+    assert abs(float(y[0, 0]) - 4096.0 * r) <= 4 * ULP32 * 4096.0 * r
+
+
 def test_rmsnorm_gamma_multiplies():
     rng = np.random.default_rng(0)
     x = F.bf16_to_f64(_bf16(rng.standard_normal((4, 128)))).astype(np.float32)
