@@ -80,13 +80,24 @@ struct WsLayout {
 
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-inline int pick_qt(int Tq, int B) { return (Tq >= 2 * B && Tq >= 4) ? 4 : 1; }
+// Four-query tiles when the queries outnumber the sequences; one-query tiles
+// for decode and whenever the query carries more than the plain number of
+// terms (the Hadamard rotation), whose larger query tile only fits beside the
+// operand ring of a one-query tile.
+inline int pick_qt(int Tq, int B, bool hadamard) {
+  return (!hadamard && Tq >= 2 * B && Tq >= 4) ? 4 : 1;
+}
+// Terms the query is carried in: bf16 caches 1 (2 with the rotation: hi and
+// lo), fp8 caches 2 e4m3 terms (3 with the rotation).
+inline int query_terms(int fmt, bool hadamard) {
+  return fmt == DSA_FMT_BF16 ? (hadamard ? 2 : 1) : (hadamard ? 3 : 2);
+}
 // selection size (the sorting networks' K) for an output of k entries
 inline int select_size(int k) { return k <= 512 ? 512 : 1024; }
 
 WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
   WsLayout L{};
-  L.QT = pick_qt(Tq, B);
+  L.QT = pick_qt(Tq, B, hadamard);
   L.NG = L.QT;  // top-k groups (one per query): merge counters per (query tile, group)
   L.G = num_sms;
   L.qtmax = (Tq + L.QT - 1) / L.QT + B;
@@ -103,9 +114,10 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
   o = up256(o + static_cast<size_t>(L.G) * 4);
   L.partials = o;
   o = up256(o + static_cast<size_t>(2) * L.G * L.QT * k * 8);
-  if (fmt == DSA_FMT_FP8 || hadamard) {  // prepared queries and head weights
+  if (fmt == DSA_FMT_FP8 || hadamard) {  // prepared queries (all terms) and head weights
     L.qh = o;
-    o = up256(o + static_cast<size_t>(Tq) * kH * kD * 2);
+    const size_t bytes_per_value = static_cast<size_t>(query_terms(fmt, hadamard)) * (fmt == DSA_FMT_BF16 ? 2 : 1);
+    o = up256(o + static_cast<size_t>(Tq) * kH * kD * bytes_per_value);
     L.wq = o;
     o = up256(o + static_cast<size_t>(Tq) * kH * 4);
   }
@@ -281,23 +293,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 // ------------------------------------------------------------------ query preparation
 // Fp8 key tiles go to the tensor cores as they are stored (kind::f8f6f4,
 // e4m3 x e4m3, both operands of one type), so each query row is split into
-// two e4m3 terms whose sum is the bf16 query: one warp per (query, head) row
-// of 128 values; a power-of-two scale 2^e puts the row's largest magnitude
-// in [2^7, 2^8); t1 = e4m3(2^e q) and t2 = e4m3(2^e q - t1), the difference
-// exact in fp32. A bf16 value has 8 significant bits and an e4m3 normal 4,
-// so t1 + t2 = 2^e q exactly whenever the remainder is not below e4m3's
-// subnormal step, i.e. for every value at least 2^-10 of the row's maximum;
-// smaller ones keep an absolute error of at most 2^-10 (scaled units).
-// Products of e4m3 operands are exact in the fp32 accumulator, and
-// w' = w * 2^-e undoes the scale after the ReLU (relu(2^e x) = 2^e relu(x)).
-// Output: t1 rows, then t2 rows, 128 bytes each.
+// e4m3 terms whose sum is the query: one warp per (query, head) row of 128
+// values; a power-of-two scale 2^e puts the row's largest magnitude in
+// [2^7, 2^8); t1 = e4m3(2^e q), t2 = e4m3(2^e q - t1), t3 = e4m3(... - t2),
+// each difference exact in fp32. A bf16 value has 8 significant bits and an
+// e4m3 normal 4, so two terms give 2^e q exactly whenever the remainder is
+// not below e4m3's subnormal step, i.e. for every value at least 2^-10 of
+// the row's maximum; smaller ones keep an absolute error of at most 2^-10
+// (scaled units). Products of e4m3 operands are exact in the fp32
+// accumulator, and w' = w * 2^-e undoes the scale after the ReLU
+// (relu(2^e x) = 2^e relu(x)).
 //
 // With the Hadamard rotation on, the row is first rotated by the same
 // unnormalised Walsh-Hadamard transform as the stored keys (fp32 butterflies
 // in the store's order: h = 1, 2 inside a lane's 4 values, h = 4 .. 64
-// between lanes l and l ^ (h/4)) and rounded to bf16, and w' carries a
-// further 2^-7 (the transform's gain 128 on the dot product); bf16 caches
-// take the rotated bf16 row as it is (E4M3 = false: 256-byte rows).
+// between lanes l and l ^ (h/4)); the rotated values are sums of up to 128
+// bf16 values and carry more bits than one bf16 or two e4m3 terms hold, so
+// they are kept as NQ terms: bf16 caches take hi = bf16(x) and
+// lo = bf16(x - hi) (16 significant bits), fp8 caches three e4m3 terms
+// (12 significant bits). w' carries a further 2^-7 (the transform's gain 128
+// on the dot product).
+// Output: term 0 rows, then term 1 rows, ... (each term [rows][128] bf16 or
+// e4m3), and w'.
 template <bool E4M3, bool HAD>
 __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
                                                     const float* __restrict__ w,
@@ -331,20 +348,27 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
         x[e] = (lane & m) ? __fsub_rn(p, x[e]) : __fadd_rn(x[e], p);
       }
     }
-    // the rotated query is a bf16 operand, like the plain one
-#pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
   }
   constexpr int kGain = HAD ? 7 : 0;  // log2 of the rotation's gain on q . k
   if constexpr (!E4M3) {
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(x[2], x[3]);
-    uint2 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&lo);
-    o.y = *reinterpret_cast<const uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(qe)[r * 32 + lane] = o;
+    // bf16 caches (only with the rotation): hi and lo bf16 terms
+    uint2 hi2, lo2;
+    {
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]);
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(x[2], x[3]);
+      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+      const __nv_bfloat162 l0 = __floats2bfloat162_rn(__fsub_rn(x[0], f0.x), __fsub_rn(x[1], f0.y));
+      const __nv_bfloat162 l1 = __floats2bfloat162_rn(__fsub_rn(x[2], f1.x), __fsub_rn(x[3], f1.y));
+      hi2.x = *reinterpret_cast<const uint32_t*>(&h0);
+      hi2.y = *reinterpret_cast<const uint32_t*>(&h1);
+      lo2.x = *reinterpret_cast<const uint32_t*>(&l0);
+      lo2.y = *reinterpret_cast<const uint32_t*>(&l1);
+    }
+    reinterpret_cast<uint2*>(qe)[r * 32 + lane] = hi2;
+    reinterpret_cast<uint2*>(qe)[(rows + r) * 32 + lane] = lo2;
     if (lane == 0) wq[r] = ldexpf(w[r], -kGain);
   } else {
+    constexpr int NQ = HAD ? 3 : 2;
     float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -354,26 +378,27 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
       frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
       e = 8 - ex;
     }
-    uint32_t t1 = 0, t2 = 0;
+    uint32_t t[NQ] = {};
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-      const float y0 = ldexpf(x[2 * p], e), y1 = ldexpf(x[2 * p + 1], e);
-      const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
-      const __half2_raw ah = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
-      const float r0 = y0 - __half2float(__ushort_as_half(ah.x));
-      const float r1 = y1 - __half2float(__ushort_as_half(ah.y));
-      const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(make_float2(r0, r1), __NV_SATFINITE, __NV_E4M3);
-      t1 |= static_cast<uint32_t>(a) << (16 * p);
-      t2 |= static_cast<uint32_t>(b) << (16 * p);
+      float y0 = ldexpf(x[2 * p], e), y1 = ldexpf(x[2 * p + 1], e);
+#pragma unroll
+      for (int term = 0; term < NQ; ++term) {
+        const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+        t[term] |= static_cast<uint32_t>(a) << (16 * p);
+        const __half2_raw ah = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
+        y0 = __fsub_rn(y0, __half2float(__ushort_as_half(ah.x)));  // exact: the remainder
+        y1 = __fsub_rn(y1, __half2float(__ushort_as_half(ah.y)));
+      }
     }
-    qe[r * 32 + lane] = t1;
-    qe[(rows + r) * 32 + lane] = t2;
+#pragma unroll
+    for (int term = 0; term < NQ; ++term) qe[(term * rows + r) * 32 + lane] = t[term];
     if (lane == 0) wq[r] = ldexpf(w[r], -e - kGain);
   }
 }
 
 // ------------------------------------------------------------------ scorer configuration
-template <int QT, int FMT, int KSEL>
+template <int QT, int FMT, int KSEL, int NQ>
 struct Cfg {
   static constexpr int N = 64 * QT;                      // MMA N: queries x heads
   static constexpr int QSW = QT == 4 ? 2 : 1;            // queries per score warp
@@ -386,7 +411,7 @@ struct Cfg {
   static constexpr int QPT = ALT ? 1 : QT / NTK;         // queries per top-k group
   static constexpr int NBUF = ALT ? 2 : QT;              // running top-k buffers
   // key-tile operand stages (32 KB bf16, 16 KB e4m3)
-  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 6) : (FMT == DSA_FMT_BF16 ? 5 : 8);
+  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 6) : (FMT == DSA_FMT_BF16 ? (NQ == 1 ? 5 : 4) : 8);
   static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
   // alternating groups each read their own ring of staging slots: a group
   // that skips the other's query tile must not wait on a slot phase that
@@ -405,7 +430,8 @@ struct Cfg {
   // trip; four-query tiles fill the 512 columns with two
   static constexpr int NTB = QT == 1 ? 4 : 2;
   static constexpr int TMEM_COLS = NTB * N;
-  static constexpr int Q_BYTES = N * 256;                 // bf16, or two e4m3 terms
+  static constexpr int TERM_BYTES = N * 128 * (FMT == DSA_FMT_BF16 ? 2 : 1);  // one query term
+  static constexpr int Q_BYTES = NQ * TERM_BYTES;
   static constexpr int OP_BYTES = kTile * (FMT == DSA_FMT_BF16 ? 256 : 128);
   static constexpr int ST_BYTES = QT * kTile * 4;        // one staged tile of scores
   static constexpr int OFF_Q = 0;
@@ -443,7 +469,7 @@ struct ScoreArgs {
   const uint8_t* cache;
   int num_pages;
   const float* w;  // head weights (prepared queries: with their scales folded in)
-  long long qrows;  // (query, head) rows; fp8: the second e4m3 term's rows follow
+  long long qrows;  // (query, head) rows; each further query term's rows follow
   const char* ws;
   WsLayout L;
   int32_t* out_idx;
@@ -886,11 +912,11 @@ __device__ __forceinline__ void write_row(const uint64_t* L, int32_t* oi, float*
 }
 
 // ------------------------------------------------------------------ the scorer
-template <int QT, int FMT, int KSEL>
-__global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
+template <int QT, int FMT, int KSEL, int NQ>
+__global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const ScoreArgs a) {
-  using C = Cfg<QT, FMT, KSEL>;
+  using C = Cfg<QT, FMT, KSEL, NQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = sm + C::OFF_Q;
@@ -977,12 +1003,16 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           *abort_flag = 1;
         } else {
           mbar_arrive_expect_tx(&ms->q_full, C::Q_BYTES);
-          if constexpr (FMT == DSA_FMT_BF16) {  // two 64-column halves
-            tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
-            tma_load_2d(sQ + C::N * 128, &tm_q, 64, s.row0 * kH, &ms->q_full);
-          } else {  // the two e4m3 terms
-            tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
-            tma_load_2d(sQ + C::N * 128, &tm_q, 0, static_cast<int>(a.qrows) + s.row0 * kH, &ms->q_full);
+#pragma unroll
+          for (int term = 0; term < NQ; ++term) {
+            const int y = static_cast<int>(term * a.qrows) + s.row0 * kH;
+            uint8_t* dq = sQ + term * C::TERM_BYTES;
+            if constexpr (FMT == DSA_FMT_BF16) {  // two 64-column halves
+              tma_load_2d(dq, &tm_q, 0, y, &ms->q_full);
+              tma_load_2d(dq + C::N * 128, &tm_q, 64, y, &ms->q_full);
+            } else {  // one 128-byte row per (query, head)
+              tma_load_2d(dq, &tm_q, 0, y, &ms->q_full);
+            }
           }
         }
         // the tile's head-weight rows into the weight buffer the epilogue
@@ -1088,18 +1118,19 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL>::NTHREADS, 1)
           const uint32_t a0 = smem_u32(sOp + slot * C::OP_BYTES);
           const uint32_t b0 = smem_u32(sQ);
           const uint32_t d = tbase + static_cast<uint32_t>(buf * C::N);
+          // the query terms accumulate into the same scores; the B operand's
+          // 128-byte-row blocks (N rows each) follow one another: bf16 terms
+          // as two 64-column halves, e4m3 terms as one 128-byte row
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < (FMT == DSA_FMT_BF16 ? 8 : 4) * NQ; ++kk) {
+            const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
             if constexpr (FMT == DSA_FMT_BF16) {
-              // K = 16 per step: two 64-column halves of 4 steps (32 B each)
-              const uint64_t ad = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32);
-              const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
+              // K = 16 per step: the key tile's two 64-column halves of 4 steps (32 B each)
+              const uint64_t ad = sw128_desc(a0 + ((kk >> 2) & 1) * 16384 + (kk & 3) * 32);
               tc_mma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
             } else {
-              // K = 32 per step over one 128-byte row; the two query terms
-              // accumulate into the same scores
+              // K = 32 per step over one 128-byte row
               const uint64_t ad = sw128_desc(a0 + (kk & 3) * 32);
-              const uint64_t bd = sw128_desc(b0 + (kk >> 2) * (C::N * 128) + (kk & 3) * 32);
               tc_mma_e4m3(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
             }
           }
@@ -1409,11 +1440,11 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-template <int QT, int FMT, int KSEL>
+template <int QT, int FMT, int KSEL, int NQ>
 dsa_status run_score(dsa_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
                      const ScoreArgs& args, int G, cudaStream_t stream) {
-  using C = Cfg<QT, FMT, KSEL>;
-  auto kern = score_kernel<QT, FMT, KSEL>;
+  using C = Cfg<QT, FMT, KSEL, NQ>;
+  auto kern = score_kernel<QT, FMT, KSEL, NQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return DSA_ERR_CUDA;
   LaunchScope scope(ctx, FMT == DSA_FMT_BF16 ? DSA_K_SCORE_BF16 : DSA_K_SCORE_FP8, stream);
@@ -1421,11 +1452,11 @@ dsa_status run_score(dsa_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
-template <int QT, int FMT>
+template <int QT, int FMT, int NQ>
 dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtensorMap& tk,
                        const ScoreArgs& args, int G, cudaStream_t stream) {
-  return k == 512 ? run_score<QT, FMT, 512>(ctx, tq, tk, args, G, stream)
-                  : run_score<QT, FMT, 1024>(ctx, tq, tk, args, G, stream);
+  return k == 512 ? run_score<QT, FMT, 512, NQ>(ctx, tq, tk, args, G, stream)
+                  : run_score<QT, FMT, 1024, NQ>(ctx, tq, tk, args, G, stream);
 }
 
 }  // namespace
@@ -1442,9 +1473,10 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
                        int32_t B, int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
                        float* out_score, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   (void)ws_bytes;
-  // tensor-map row coordinates are 32-bit: (query, head) rows, and for fp8
-  // both query terms, must stay below 2^31
-  if (static_cast<long long>(Tq) * kH * 2 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
+  // tensor-map row coordinates are 32-bit: the (query, head) rows of every
+  // query term must stay below 2^31
+  if (static_cast<long long>(Tq) * kH * query_terms(fmt, ctx->hadamard != 0) > 0x7FFFFFFFLL)
+    return DSA_ERR_UNSUPPORTED;
   // any k <= 1024 runs the top-512 or top-1024 selection and writes the
   // first k entries of each sorted row
   const int ksel = select_size(k);
@@ -1481,8 +1513,9 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
 
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(ctx->encode_tiled);
   CUtensorMap tq, tk;
-  if (fmt == DSA_FMT_BF16) {  // [rows x 128] bf16, boxes of 64 columns
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const int nq = query_terms(fmt, ctx->hadamard != 0);
+  if (fmt == DSA_FMT_BF16) {  // [nq * rows x 128] bf16 (the terms one after the other), boxes of 64 columns
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(nq * rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD * 2)};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(64 * L.QT)};
     const cuuint32_t estr[2] = {1, 1};
@@ -1490,8 +1523,8 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return DSA_ERR_CUDA;
-  } else {  // [2 * rows x 128] e4m3: first terms, then second terms
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(2 * rows)};
+  } else {  // [nq * rows x 128] e4m3: first terms, then second terms, ...
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(nq * rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
     const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(64 * L.QT)};
     const cuuint32_t estr[2] = {1, 1};
@@ -1536,11 +1569,14 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   args.out_score = out_score;
   args.status = ctx->status;
   const int G = L.G;
+  if (ctx->hadamard)  // one-query tiles (pick_qt), one more query term
+    return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream)
+                               : run_score_k<1, DSA_FMT_FP8, 3>(ctx, ksel, tq, tk, args, G, stream);
   if (L.QT == 4)
-    return fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16>(ctx, ksel, tq, tk, args, G, stream)
-                               : run_score_k<4, DSA_FMT_FP8>(ctx, ksel, tq, tk, args, G, stream);
-  return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16>(ctx, ksel, tq, tk, args, G, stream)
-                             : run_score_k<1, DSA_FMT_FP8>(ctx, ksel, tq, tk, args, G, stream);
+    return fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
+                               : run_score_k<4, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+  return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
+                             : run_score_k<1, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
 }
 
 }  // namespace dsa

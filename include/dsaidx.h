@@ -123,12 +123,14 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
  * order (entries +-1, fp32 butterflies h = 1, 2, ..., 64, each pair
  * (i, i+h) -> (a + b, a - b)), and dsa_index_topk rotates every query head by
  * the same H and divides the dot products by 128, so scores keep their
- * meaning: (H q) . (H k) / 128 = q . k. The rotated query is rounded to bf16,
- * the precision of the plain query (fp8 caches then split it into two e4m3
- * terms as usual).
+ * meaning: (H q) . (H k) / 128 = q . k. The query is rotated exactly, as far
+ * as the scores can tell: the fp32 rotation is carried as two bf16 terms
+ * (hi + lo, 16 significant bits) for bf16 caches and three e4m3 terms (12
+ * bits) for fp8 caches, each term its own pass of the tensor cores, and the
+ * queries run in one-query tiles.
  * A cache must be written and read with the same setting. Off by default;
  * applies to the calls made after it, and changes the size
- * dsa_index_topk_workspace_size reports for bf16 caches. */
+ * dsa_index_topk_workspace_size reports. */
 dsa_status dsa_ctx_set_hadamard(dsa_ctx* ctx, int32_t on);
 
 /* Slot output: when on, dsa_index_topk writes into out_idx the cache slot of
@@ -167,7 +169,8 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  *  cu_q        (device) [B+1] int32, cu_q[0] = 0, non-decreasing, cu_q[B] = Tq.
  *  k           1 .. 1024 (the pages use 512 and 1024; other k run the top-512
  *              or top-1024 selection and keep the first k of each sorted
- *              row).  B <= 16384, Tq < 2^24 (else DSA_ERR_UNSUPPORTED).
+ *              row).  B <= 16384 and Tq < 2^24 (2^31 / 192 with the Hadamard
+ *              rotation on an fp8 cache), else DSA_ERR_UNSUPPORTED.
  *  out_idx     (device) [Tq][k] int32;  out_score (device) [Tq][k] fp32.
  *  workspace   (device) >= dsa_index_topk_workspace_size(...) bytes, 256-byte
  *              aligned; contents need not be initialised and are scratch.

@@ -1,10 +1,12 @@
 """Helpers for the GPU tests: move a synthetic workload to the device, run the
-library through its binding, and run the oracle on the same inputs."""
+library through its binding, and run the oracle on the same inputs (the C++
+oracle for speed; the numpy oracle on request)."""
 from __future__ import annotations
 
 import numpy as np
 
 from oracle import indexer as X
+from oracle import native as N
 from oracle import store as S
 
 
@@ -54,17 +56,45 @@ def run_topk(wl, fmt, ctx, d, k=None):
     return out_i.cpu().numpy(), out_s.cpu().numpy()
 
 
-def oracle_cache(wl, fmt):
+def oracle_cache(wl, fmt, native=True):
+    """The oracle's byte image of the cache after the workload's stores (the
+    C++ oracle by default; its bytes equal the numpy oracle's, which
+    tests/test_oracle_native.py pins)."""
     c = S.new_cache(wl.num_pages, fmt)
-    S.store(c, fmt, wl.fill_k, wl.fill_pos, wl.fill_seq, wl.page_table, wl.num_pages, wl.theta, wl.eps)
-    S.store(c, fmt, wl.new_k, wl.new_pos, wl.new_seq, wl.page_table, wl.num_pages, wl.theta, wl.eps)
+    st = N.store if native else S.store
+    st(c, fmt, wl.fill_k, wl.fill_pos, wl.fill_seq, wl.page_table, wl.num_pages, wl.theta, wl.eps)
+    st(c, fmt, wl.new_k, wl.new_pos, wl.new_seq, wl.page_table, wl.num_pages, wl.theta, wl.eps)
     return c
 
 
-def oracle_topk(wl, fmt, cache, rows, k=None):
+def oracle_topk(wl, fmt, cache, rows, k=None, native=True, hadamard=False):
+    """Oracle top-k of the given rows with their full score vectors (the C++
+    oracle by default)."""
     k = wl.k if k is None else k
-    return X.index_topk(cache, fmt, wl.page_table, wl.seq_lens, wl.cu_q, wl.q, wl.head_w,
-                        wl.causal, k, rows=rows, return_scores=True)
+    f = N.index_topk if native else X.index_topk
+    return f(cache, fmt, wl.page_table, wl.seq_lens, wl.cu_q, wl.q, wl.head_w, wl.causal, k,
+             rows=rows, return_scores=True, hadamard=hadamard)
+
+
+def compare_all_rows(wl, fmt, cache, gi, gs, rows=None, k=None, block=1024, hadamard=False):
+    """Compare the GPU's rows with the C++ oracle block by block (so the full
+    score vectors of a long prefill never sit in memory at once). Returns
+    (ok, summary over all rows)."""
+    from tests import parity as P
+    k = wl.k if k is None else k
+    rows = np.arange(wl.Tq) if rows is None else np.asarray(rows)
+    bad, n, swaps, err = [], 0, 0, 0.0
+    for i0 in range(0, len(rows), block):
+        rr = rows[i0:i0 + block]
+        oi, os_, full = oracle_topk(wl, fmt, cache, rr, k, hadamard=hadamard)
+        ok, reps = P.compare(rr, gi[rr], gs[rr], oi, os_, full, k, fmt)
+        n += len(reps)
+        swaps += sum(r.swaps for r in reps)
+        err = max(err, max((r.logit_err for r in reps), default=0.0))
+        bad += [r for r in reps if not r.ok]
+    summ = {"rows": n, "failed": len(bad), "swaps": int(swaps), "max_logit_err": err,
+            "first_failure": None if not bad else f"row {bad[0].row}: {bad[0].why}"}
+    return not bad, summ
 
 
 def slot_bytes(cache_np: np.ndarray, fmt: int, wl, pos, seq):

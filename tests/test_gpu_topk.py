@@ -3,8 +3,11 @@
 Rules (tests/parity.py): equal top-k sets except swaps within 1e-3 * max|s|
 of the oracle's k-th score; logits within 2e-3 (bf16) / 3e-2 (fp8) of the
 oracle relative to the row's largest top-k score; rows sorted by (score
-desc, position asc); -1 / -inf padding.
+desc, position asc); -1 / -inf padding. Every row of every workload is
+compared, the five workloads included, against the C++ oracle.
 """
+import functools
+
 import numpy as np
 import pytest
 
@@ -17,6 +20,13 @@ from tests import parity as P
 pytestmark = pytest.mark.gpu
 
 FMTS = [S.FMT_BF16, S.FMT_FP8]
+
+
+@functools.lru_cache(maxsize=None)
+def _workload(name):
+    """The named workload, generated once per test session (the long ones
+    take seconds to draw)."""
+    return I.WORKLOADS[name]()
 
 
 @pytest.fixture(scope="module")
@@ -34,12 +44,10 @@ def _check(wl, fmt, ctx, rows=None, k=None):
     d = U.device_workload(wl, fmt, ctx)
     gi, gs = U.run_topk(wl, fmt, ctx, d, k)
     assert ctx.device_status() == 0
-    rows = np.arange(wl.Tq) if rows is None else np.asarray(rows)
     cache = U.oracle_cache(wl, fmt)
-    oi, os_, full = U.oracle_topk(wl, fmt, cache, rows, k)
-    ok, reps = P.compare(rows, gi[rows], gs[rows], oi, os_, full, k, fmt)
-    assert ok, P.summary(reps)
-    return gi, gs, reps
+    ok, summ = U.compare_all_rows(wl, fmt, cache, gi, gs, rows, k)
+    assert ok, summ
+    return gi, gs, summ
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -99,40 +107,43 @@ def test_sequence_without_queries_and_mixed_counts(ctx):
 @pytest.mark.parametrize("fmt", FMTS)
 def test_tiny_prefill_config(ctx, fmt):
     # 1 sequence, 1024 tokens, all queries causal, k=512 (the smallest workload)
-    _check(I.tiny_prefill(), fmt, ctx)
+    _check(_workload("tiny_prefill"), fmt, ctx)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_batched_decode_config(ctx, fmt):
     # 64 sequences x 1 query, contexts U[2048, 16384], permuted pages, k=512
-    _check(I.batched_decode(), fmt, ctx)
+    _check(_workload("batched_decode"), fmt, ctx)
 
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_needle_config(ctx, fmt):
-    wl = I.needle()
-    rows = np.concatenate([np.array(wl.needle_queries), np.arange(0, wl.Tq - 64, 331)])
-    gi, _, _ = _check(wl, fmt, ctx, rows=rows)
+    # every row of the 10498-token needle prefill; each planted needle is in
+    # the top-k of every query that carries the needle direction
+    wl = _workload("needle")
+    gi, _, summ = _check(wl, fmt, ctx)
+    assert summ["rows"] == wl.Tq
     for r in wl.needle_queries:
         sel = set(gi[r].tolist())
         for p in wl.needles:
             assert p in sel, f"needle at {p} missing for query {r}"
 
 
-def test_long_prefill_config_sampled(ctx):
-    # the 22528-token causal prefill: sampled rows against the oracle, and
-    # the scratch stays O(#SMs * tile + Tq * k)
-    import torch
-    wl = I.long_prefill()
-    ws = ctx.topk_workspace_size(wl.Tq, wl.B, wl.k, 0)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_long_prefill_config(ctx, fmt):
+    # the 22528-token causal prefill, every row against the C++ oracle; the
+    # scratch stays O(#SMs * tile + Tq * k), far below the 1.89 GiB of one
+    # fp32 [L x L] logits buffer
+    wl = _workload("long_prefill")
+    ws = ctx.topk_workspace_size(wl.Tq, wl.B, wl.k, fmt)
     assert ws < 64 << 20
-    rng = np.random.default_rng(0)
-    rows = np.sort(np.concatenate([[0, 1, 127, 128, 511, 512, 513, wl.Tq - 1],
-                                   rng.choice(wl.Tq, 40, replace=False)]))
-    _check(wl, 0, ctx, rows=rows)
+    _, _, summ = _check(wl, fmt, ctx)
+    assert summ["rows"] == wl.Tq
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_long_decode_config_sampled(ctx, fmt):
-    wl = I.long_decode()
-    _check(wl, fmt, ctx, rows=np.arange(wl.Tq))
+def test_long_decode_config(ctx, fmt):
+    # 8 sequences at 131072 tokens (1.05M pre-filled + 2048 appended), 8
+    # queries each, k = 1024: every row
+    wl = _workload("long_decode")
+    _check(wl, fmt, ctx)
