@@ -22,11 +22,13 @@
 //           of their key-tile counts, and each CTA's first query tile, so the
 //           CTAs split the total work evenly with one dependent load.
 //   qprep   fp8 caches or Hadamard rotation only: q rotated (if on) and, for
-//           fp8 caches, split into two e4m3 terms with a power-of-two scale
-//           per (query, head), the scales folded into the head weights, so
-//           the tensor cores take the stored e4m3 keys as they are.
+//           fp8 caches, split into e4m3 terms with a power-of-two scale per
+//           (query, head), the scales folded into the head weights, so the
+//           tensor cores take the stored e4m3 keys as they are.
 //   score   persistent, one CTA per SM, warp-specialised:
 //             warp 0      producer: page-table lookups, TMA of 64-token pages
+//                         (and, for fp8 one-query tiles, a bulk copy of the
+//                         pages' scales into a ring of their own)
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
 //                         x K=128 into a ring of TMEM accumulators (4 for
 //                         one-query tiles, 2 for four-query tiles)
@@ -34,14 +36,14 @@
 //                         scale, mask; one score per key staged in a ring of
 //                         shared-memory slots
 //             top-k groups of 4 warps: threshold filter of the staged scores
-//                         into a running top-k per query (one-query tiles:
-//                         two groups on alternate query tiles, each merging
-//                         candidate batches into a sorted list; four-query
-//                         tiles: one group per query, a buffer cut back by
-//                         radix select and sorted at the end); then output
-//                         (or, for a query tile split across CTAs, a sorted
-//                         partial list, merged by the piece that finishes
-//                         last)
+//                         into a candidate buffer per query, cut back by
+//                         radix select when full and at the end, then sorted
+//                         (one-query tiles: two groups on alternate query
+//                         tiles; four-query tiles: one group per query);
+//                         then output (or, for a query tile split across
+//                         CTAs, a sorted partial list, merged by the piece
+//                         that finishes last; its pieces share a running
+//                         threshold per query)
 //           Keys sit on the MMA's M dimension so each score thread owns one
 //           key (one TMEM lane) and reduces over heads in its own registers.
 #include <cuda_bf16.h>
@@ -74,7 +76,7 @@ struct PlanHdr {
 // Per query tile: {b, row0, nrows, ntile} and {L, qpos0, 0, 0} where qpos0 is
 // the position of the tile's first query.
 struct WsLayout {
-  size_t hdr, meta, prefix, counters, rec, partials, qh, wq, total;
+  size_t hdr, meta, prefix, counters, rec, partials, gthr, qh, wq, total;
   int QT, G, qtmax, NG;
 };
 
@@ -114,6 +116,8 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
   o = up256(o + static_cast<size_t>(L.G) * 4);
   L.partials = o;
   o = up256(o + static_cast<size_t>(2) * L.G * L.QT * k * 8);
+  L.gthr = o;  // per query row: the largest running k-th key published by its pieces
+  o = up256(o + static_cast<size_t>(Tq) * 8);
   if (fmt == DSA_FMT_FP8 || hadamard) {  // prepared queries (all terms) and head weights
     L.qh = o;
     const size_t bytes_per_value = static_cast<size_t>(query_terms(fmt, hadamard)) * (fmt == DSA_FMT_BF16 ? 2 : 1);
@@ -175,6 +179,19 @@ __device__ __forceinline__ long long range_start(int c, long long total, int G) 
   return static_cast<long long>(c) * total / G;
 }
 
+__device__ __forceinline__ int owner_of(long long gtile, long long total, int G) {
+  int c = static_cast<int>(gtile * G / total);
+  while (c + 1 < G && range_start(c + 1, total, G) <= gtile) ++c;
+  while (c > 0 && range_start(c, total, G) > gtile) --c;
+  return c;
+}
+// A CTA keeps at most two partial lists: slot 2c for the query tile its
+// range starts in, 2c+1 for the one it ends in.
+__device__ __forceinline__ int partial_slot(int c, long long qt_start, long long total, int G) {
+  return range_start(c, total, G) >= qt_start ? 2 * c : 2 * c + 1;
+}
+
+
 // ------------------------------------------------------------------ plan
 // One CTA. Per-sequence sizes and query-tile offsets live in shared memory
 // (B <= kMaxSeqs), so the only global round trips are the input loads and
@@ -199,6 +216,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   long long* prefix = reinterpret_cast<long long*>(ws + L.prefix);
   int* cnt = reinterpret_cast<int*>(ws + L.counters);
   int* rec = reinterpret_cast<int*>(ws + L.rec);
+  unsigned long long* gthr = reinterpret_cast<unsigned long long*>(ws + L.gthr);
 
   for (int i = threadIdx.x; i <= B; i += 1024) {
     s_cq[i] = cu_q[i];
@@ -256,6 +274,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     if (qt < qtot) {
       prefix[qt] = lcarry + ex;
       for (int g = 0; g < NG; ++g) cnt[qt * NG + g] = 0;
+      for (int r = 0; r < m.z; ++r) gthr[m.y + r] = 0ull;
       if (m.w == 0) {  // no visible keys: the rows are all padding
         for (int r = 0; r < m.z; ++r)
           for (int i = 0; i < k; ++i) {
@@ -276,10 +295,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     hdr->ovh = ovh;
   }
   __syncthreads();
-  // first query tile of each CTA: the non-empty tile holding its range start
+  // first query tile of each CTA: the non-empty tile holding its range start;
+  // and each query tile's first and last CTA with key tiles of it
   for (int qt = threadIdx.x; qt < qtot; qt += 1024) {
     const long long p0 = prefix[qt], p1 = prefix[qt + 1];
     if (p1 <= p0) continue;
+    meta[2 * qt + 1].z = owner_of(p0 + ovh, total, Ge);
+    meta[2 * qt + 1].w = owner_of(p1 - 1, total, Ge);
     int c = static_cast<int>(p0 * Ge / total);
     while (c > 0 && range_start(c, total, Ge) >= p0) --c;
     for (; c < Ge; ++c) {
@@ -410,17 +432,19 @@ struct Cfg {
   static constexpr int NTK = ALT ? 2 : QT;
   static constexpr int QPT = ALT ? 1 : QT / NTK;         // queries per top-k group
   static constexpr int NBUF = ALT ? 2 : QT;              // running top-k buffers
-  // key-tile operand stages (32 KB bf16, 16 KB e4m3)
-  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 6) : (FMT == DSA_FMT_BF16 ? (NQ == 1 ? 5 : 4) : 8);
+  // key-tile operand stages (32 KB bf16, 16 KB e4m3): enough bytes in flight
+  // per SM to cover the HBM latency of a streaming one-query tile
+  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 6) : (FMT == DSA_FMT_BF16 ? 4 : 6);
   static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
   // alternating groups each read their own ring of staging slots: a group
   // that skips the other's query tile must not wait on a slot phase that
   // the score warps have not reached yet
   static constexpr int NRING = ALT ? 2 : 1;
   static constexpr int RS = NST / NRING;                 // slots per ring
-  // keys of one query's running top-k: sorted list + batch of KSEL each
-  // (one-query tiles), else a candidate buffer cut back by radix select
-  static constexpr int TK = ALT ? 2 * KSEL : 1280;
+  // candidate keys of one query's running top-k, cut back to KSEL by radix
+  // select when full: one-query tiles get a buffer large enough that a
+  // CTA's piece of a decode query usually needs one selection, at its end
+  static constexpr int TK = ALT ? (FMT == DSA_FMT_BF16 && NQ == 2 ? 3072 : 4096) : 1280;
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
   static constexpr int NWARPS = W_TOPK + 4 * NTK;
@@ -440,11 +464,18 @@ struct Cfg {
   static constexpr int OFF_ST = OFF_TOPK + NBUF * TK * 8;
   static constexpr int OFF_W = OFF_ST + NST * ST_BYTES;
   static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;   // head weights, double-buffered
-  static constexpr int OFF_MISC = OFF_HIST + (ALT ? 0 : NTK * 512 * 4);  // radix-select histograms
+  // fp8 key scales of one-query tiles: the 2 x 64 fp32 scales of a tile's two
+  // pages come into a ring of their own by bulk copy beside the codes (the
+  // score warps read them after the MMA has released the operand stage);
+  // four-query tiles are slow enough per tile to load them from global memory
+  static constexpr bool SCALE_RING = FMT == DSA_FMT_FP8 && QT == 1;
+  static constexpr int NSC = SCALE_RING ? 16 : 0;          // scale slots (tiles)
+  static constexpr int OFF_SC = OFF_HIST + NTK * 512 * 4;  // after the radix-select histograms
+  static constexpr int OFF_MISC = OFF_SC + NSC * kTile * 4;
   static constexpr int MISC_BYTES = 2048;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(ALT || (TK % 128 == 0 && TK >= KSEL + 128), "candidate buffer");
+  static_assert(TK % 128 == 0 && TK >= KSEL + 128, "candidate buffer");
   static_assert(NTHREADS <= 1024, "block size");
 };
 
@@ -452,6 +483,7 @@ struct Misc {
   uint64_t op_full[8], op_empty[8];
   uint64_t tm_full[4], tm_empty[4], q_full, q_empty, fin, w_full[2], w_empty[2];
   uint64_t st_full[16], st_empty[16];
+  uint64_t sc_full[16], sc_empty[16];
   uint32_t tmem_base;
   int abort;
   int cnt[4];
@@ -540,33 +572,17 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ int owner_of(long long gtile, long long total, int G) {
-  int c = static_cast<int>(gtile * G / total);
-  while (c + 1 < G && range_start(c + 1, total, G) <= gtile) ++c;
-  while (c > 0 && range_start(c, total, G) > gtile) --c;
-  return c;
-}
-// A CTA keeps at most two partial lists: slot 2c for the query tile its
-// range starts in, 2c+1 for the one it ends in.
-__device__ __forceinline__ int partial_slot(int c, long long qt_start, long long total, int G) {
-  return range_start(c, total, G) >= qt_start ? 2 * c : 2 * c + 1;
-}
-
 // ------------------------------------------------------------------ running top-k (one group of 128 threads)
-// Keys above a query's threshold are appended to a shared-memory buffer as
-// tiles arrive. Two ways to keep the buffer bounded:
-//   * list + batch (one-query tiles): the running top-k is a list L of K keys
-//     sorted in descending order (key 0 marks an empty slot); a nearly full
-//     batch of candidates is sorted and merged into L with bitonic networks
-//     and L's K-th key becomes the threshold. The end of a query tile then
-//     costs one partial batch, which matters when a CTA finishes few tiles.
-//   * radix select (several queries per tile): a full buffer is cut back to
-//     its K largest keys; the rare large compactions are cheaper than many
-//     batch merges when four groups share the SM with busy score warps, and
-//     the keys are sorted once at the end.
+// Keys above a query's threshold are appended to a shared-memory candidate
+// buffer as tiles arrive. A full buffer is cut back to its K largest keys by
+// a radix select, whose K-th key becomes the threshold; at the end of the
+// query tile the buffer is cut back once more and the K keys are sorted.
+// The buffer is large next to K, so the selections are few: one-query tiles
+// (decode) have one 4096-key buffer per group and a CTA's piece of a decode
+// query usually needs a single selection, at its end.
 //
-// The networks run in registers over K slots held by the group's 4 warps:
-// slot x = w*PW + lane*E + e is register e of lane `lane` of warp w
+// The sorting networks run in registers over K slots held by the group's 4
+// warps: slot x = w*PW + lane*E + e is register e of lane `lane` of warp w
 // (PW = K/4, E = K/128). Strides below E stay inside a thread, strides up
 // to PW use shuffles, larger ones (between warps) go through a K-key
 // shared-memory exchange buffer.
@@ -809,39 +825,6 @@ __device__ __forceinline__ void net_merge(uint64_t (&v)[K / 128], uint64_t* xbuf
   for (int stride = K >> 1; stride > 0; stride >>= 1) net_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
 }
 
-// L := the K largest of L and batch[0..*cnt) (*cnt <= K); *thr := L's
-// K-th key (0 while L has empty slots); *cnt := 0. The batch buffer (K
-// keys) is the exchange buffer of the networks. The larger half of the
-// union is the elementwise maximum of the sorted batch and L reversed, a
-// bitonic sequence, so one merge network sorts it. Kept out of line: one
-// copy of the networks' code serves every call site.
-template <int K>
-__device__ __noinline__ void batch_merge(uint64_t* batch, int* cnt, uint64_t* L, unsigned long long* thr,
-                                         int gt, int barid) {
-  constexpr int PW = K / 4, E = PW / 32;
-  const int w = gt >> 5, lane = gt & 31;
-  const int n = *cnt;
-  uint64_t v[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {  // the batch is unordered: any slot assignment
-    const int x = w * PW + e * 32 + lane;
-    v[e] = x < n ? batch[x] : 0ull;
-  }
-  net_sort<K>(v, batch, w, lane, barid);
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const uint64_t o = L[K - 1 - (w * PW + lane * E + e)];
-    v[e] = v[e] > o ? v[e] : o;
-  }
-  net_merge<K>(v, batch, w, lane, barid);
-  named_bar(barid, 128);  // every read of L is done
-#pragma unroll
-  for (int e = 0; e < E; ++e) L[w * PW + lane * E + e] = v[e];
-  if (gt == 127) *thr = v[E - 1];
-  if (gt == 0) *cnt = 0;
-  named_bar(barid, 128);
-}
-
 // Sort buf[0..n) (n <= K, distinct keys) into buf[0..K) descending, 0 in
 // the slots past n. buf (at least K keys) is the exchange buffer.
 template <int K>
@@ -924,6 +907,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
   uint64_t* sTopk = reinterpret_cast<uint64_t*>(sm + C::OFF_TOPK);
   float* sW = reinterpret_cast<float*>(sm + C::OFF_W);
   float* sSt = reinterpret_cast<float*>(sm + C::OFF_ST);
+  float* sSc = reinterpret_cast<float*>(sm + C::OFF_SC);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(sm + C::OFF_HIST);
   Misc* ms = reinterpret_cast<Misc*>(sm + C::OFF_MISC);
 
@@ -942,6 +926,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ms->st_full[i], C::NSW);
       mbar_init(&ms->st_empty[i], C::ALT ? 4 : 4 * C::NTK);
+    }
+    for (int i = 0; i < C::NSC; ++i) {
+      mbar_init(&ms->sc_full[i], 1);
+      mbar_init(&ms->sc_empty[i], C::NSW);
     }
     mbar_init(&ms->q_full, 1);
     mbar_init(&ms->q_empty, 1);
@@ -1069,10 +1057,24 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
                 tma_load_2d(dst + 16384 + 8192, &tm_k, 64, p1 * 64, &ms->op_full[slot]);
               }
             } else {
-              // a page = 64 keys x 128 e4m3 bytes, the scales after it stay
+              // a page = 64 keys x 128 e4m3 bytes (its 64 scales follow it)
               mbar_arrive_expect_tx(&ms->op_full[slot], (v0 + v1) * 8192);
               if (v0) tma_load_3d(dst, &tm_k, 0, 0, p0, &ms->op_full[slot]);
               if (v1) tma_load_3d(dst + 8192, &tm_k, 0, 0, p1, &ms->op_full[slot]);
+            }
+          }
+          if constexpr (C::SCALE_RING) {
+            // the two pages' 256-byte scale blocks into the tile's scale slot
+            const int ss = tile_seq % C::NSC, us = tile_seq / C::NSC;
+            if (!*abort_flag && !mbar_wait(&ms->sc_empty[ss], (us & 1) ^ 1)) {
+              atomicOr(a.status, DSA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+            if (!*abort_flag) {
+              mbar_arrive_expect_tx(&ms->sc_full[ss], (v0 + v1) * 256);
+              const uint8_t* sb = a.cache + 64 * 128;
+              if (v0) bulk_load(sSc + ss * kTile, sb + static_cast<long long>(p0) * kPageBytesFp8, 256, &ms->sc_full[ss]);
+              if (v1) bulk_load(sSc + ss * kTile + 64, sb + static_cast<long long>(p1) * kPageBytesFp8, 256, &ms->sc_full[ss]);
             }
           }
         }
@@ -1085,6 +1087,12 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
       for (int i = 1; i <= C::S && tile_seq - i >= 0; ++i) {
         const int ts = tile_seq - i;
         mbar_wait(&ms->op_full[ts % C::S], (ts / C::S) & 1, 20000000LL);
+      }
+      if constexpr (C::SCALE_RING) {
+        for (int i = 1; i <= C::NSC && tile_seq - i >= 0; ++i) {
+          const int ts = tile_seq - i;
+          mbar_wait(&ms->sc_full[ts % C::NSC], (ts / C::NSC) & 1, 20000000LL);
+        }
       }
       mbar_wait(&ms->q_full, (seg_i - 1) & 1, 20000000LL);
       if (seg_i > 0) mbar_wait(&ms->w_full[(seg_i - 1) & 1], ((seg_i - 1) >> 1) & 1, 20000000LL);
@@ -1181,7 +1189,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
         return (v < 0 || v >= a.num_pages) ? -1 : v;
       };
       auto scale_of = [&](int id, int tt) -> float {
-        if constexpr (FMT == DSA_FMT_FP8) {
+        if constexpr (FMT == DSA_FMT_FP8 && !C::SCALE_RING) {
           if (id >= 0)
             return __ldg(reinterpret_cast<const float*>(a.cache + static_cast<long long>(id) * kPageBytesFp8 +
                                                         64 * 128 + ((tt * kTile + row) & 63) * 4));
@@ -1210,6 +1218,21 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           break;
         }
         tc_fence_after();
+        float rscale = 1.f;  // this key's fp8 scale, from the scale ring
+        if constexpr (C::SCALE_RING) {
+          const int ss = tile_seq % C::NSC, uss = tile_seq / C::NSC;
+          if (!__all_sync(0xffffffffu, mbar_wait(&ms->sc_full[ss], uss & 1))) {
+            if (lane == 0) {
+              atomicOr(a.status, DSA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+            stop = true;
+            break;
+          }
+          rscale = sSc[ss * kTile + row];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ms->sc_empty[ss]);
+        }
         float scs[C::QSW];
 #pragma unroll
         for (int jj = 0; jj < C::QSW; ++jj) {
@@ -1241,7 +1264,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) unpack2(a2[i], acc[2 * i], acc[2 * i + 1]);
           float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-          if constexpr (FMT == DSA_FMT_FP8) sc *= kscale;
+          if constexpr (FMT == DSA_FMT_FP8) sc *= C::SCALE_RING ? rscale : kscale;
           const int lim = j < s.nrows ? (a.causal ? s.qpos0 + j + 1 : s.L) : 0;
           if (pid < 0 || pos >= lim) sc = -__int_as_float(0x7f800000);
           scs[jj] = sc;
@@ -1273,7 +1296,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile (of
     // every other query tile, query 0, when the tiles hold one query): it
     // filters the staged scores against each query's threshold into its
-    // candidate buffer, bounds the buffer (batch merge or radix select), and
+    // candidate buffer, bounds the buffer (radix select), and
     // at the end of the query tile leaves the sorted top-k in the first KSEL
     // slots and writes the row (or publishes the sorted list of its piece of
     // the keys and, if it is the last piece to finish, merges all pieces).
@@ -1285,6 +1308,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     Seg s;
     bool stop = false;
     int* counters = reinterpret_cast<int*>(const_cast<char*>(a.ws) + a.L.counters);
+    unsigned long long* gthr = reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.gthr);
     unsigned long long* partials =
         reinterpret_cast<unsigned long long*>(const_cast<char*>(a.ws) + a.L.partials);
     // query jj of this group in the tile, its running top-k and where its
@@ -1292,14 +1316,23 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     auto qrow = [&](int jj) { return C::ALT ? jj : tg * C::QPT + jj; };
     auto qlist = [&](int jj) { return sTopk + (C::ALT ? tg : tg * C::QPT + jj) * C::TK; };
     auto qbuf = [&](int jj) { return C::ALT ? tg : tg * C::QPT + jj; };
-    auto qcand = [&](int jj) { return qlist(jj) + (C::ALT ? KSEL : 0); };
     // page-table row for slot output (null: positions)
     auto out_pt = [&](const Seg& sg) -> const int32_t* {
       return a.slots ? a.page_table + static_cast<long long>(sg.b) * a.max_pages : nullptr;
     };
     while (!stop && it.next(s)) {
       if (C::ALT && (seg_i++ & 1) != tg) continue;  // the other group's query tile
+      // A query tile whose keys are split over several CTAs shares one
+      // threshold per query: each piece publishes its running k-th key
+      // (atomicMax) and filters against the largest one published. A key
+      // below another piece's k-th key has k keys above it already, so it
+      // cannot be in the query's top-k; the pieces' lists still hold every
+      // key that is. The shared word is touched only when a piece's own
+      // threshold has changed (after a selection), never per tile: other
+      // pieces hammer the same word.
+      const bool share = !s.whole;
       unsigned long long thr[C::QPT];
+      int nsel[C::QPT];  // selections so far
 #pragma unroll
       for (int jj = 0; jj < C::QPT; ++jj) {
         const int jb = qbuf(jj);
@@ -1307,12 +1340,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           ms->cnt[jb] = 0;
           ms->thr[jb] = 0;
         }
-        if constexpr (C::ALT) {
-          uint64_t* L = qlist(jj);
-#pragma unroll
-          for (int i = 0; i < KSEL / 128; ++i) L[i * 128 + gt] = 0ull;
-        }
         thr[jj] = 0;
+        nsel[jj] = 0;
       }
       if (gt == 0) ms->gok[tg] = 1;
       named_bar(barid, 128);
@@ -1328,7 +1357,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
             const float sc = sSt[st * (QT * kTile) + j * kTile + gt];
             const uint64_t key = make_key(sc, pos);
             const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
-            push_key(pass, key, qcand(jj), &ms->cnt[jb], lane);
+            push_key(pass, key, qlist(jj), &ms->cnt[jb], lane);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->st_empty[st]);
@@ -1345,15 +1374,24 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
           const int jb = qbuf(jj);
-          // make room before the next tile could overflow the buffer
-          if constexpr (C::ALT) {
-            if (ms->cnt[jb] > KSEL - kTile)
-              batch_merge<KSEL>(qcand(jj), &ms->cnt[jb], qlist(jj), &ms->thr[jb], gt, barid);
-          } else {
-            if (ms->cnt[jb] > C::TK - kTile)
-              group_compact(qcand(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+          // make room before the next tile could overflow the buffer; the
+          // first selection of a one-query tile comes at 2 KSEL candidates,
+          // early enough that its threshold keeps the buffer (and the
+          // piece's last selection) small
+          const int limit = (C::ALT && nsel[jj] == 0) ? 2 * KSEL : C::TK;
+          if (ms->cnt[jb] > limit - kTile) {
+            group_compact(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+            ++nsel[jj];
+            unsigned long long t_new = ms->thr[jb];
+            const int j = qrow(jj);
+            if (share && j < s.nrows) {
+              unsigned long long* g = gthr + s.row0 + j;
+              if (gt == 0) atomicMax(g, t_new);
+              const unsigned long long gv = __ldcg(g);
+              t_new = gv > t_new ? gv : t_new;
+            }
+            thr[jj] = t_new > thr[jj] ? t_new : thr[jj];
           }
-          thr[jj] = ms->thr[jb];
         }
         ++tile_seq;
       }
@@ -1363,13 +1401,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
 #pragma unroll
       for (int jj = 0; jj < C::QPT; ++jj) {
         const int jb = qbuf(jj);
-        if constexpr (C::ALT) {
-          if (ms->cnt[jb] > 0)
-            batch_merge<KSEL>(qcand(jj), &ms->cnt[jb], qlist(jj), &ms->thr[jb], gt, barid);
-        } else {
-          group_compact(qcand(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
-          if (qrow(jj) < s.nrows) sort_list<KSEL>(qlist(jj), min(ms->cnt[jb], KSEL), gt, barid);
-        }
+        group_compact(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+        if (share && gt == 0 && qrow(jj) < s.nrows) atomicMax(gthr + s.row0 + qrow(jj), ms->thr[jb]);
+        if (qrow(jj) < s.nrows) sort_list<KSEL>(qlist(jj), min(ms->cnt[jb], KSEL), gt, barid);
       }
       if (s.whole) {
 #pragma unroll
@@ -1569,14 +1603,17 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   args.out_score = out_score;
   args.status = ctx->status;
   const int G = L.G;
+  dsa_status st;
   if (ctx->hadamard)  // one-query tiles (pick_qt), one more query term
-    return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream)
-                               : run_score_k<1, DSA_FMT_FP8, 3>(ctx, ksel, tq, tk, args, G, stream);
-  if (L.QT == 4)
-    return fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
-                               : run_score_k<4, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
-  return fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
+    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream)
+                             : run_score_k<1, DSA_FMT_FP8, 3>(ctx, ksel, tq, tk, args, G, stream);
+  else if (L.QT == 4)
+    st = fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
+                             : run_score_k<4, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+  else
+    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
                              : run_score_k<1, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+  return st;
 }
 
 }  // namespace dsa
