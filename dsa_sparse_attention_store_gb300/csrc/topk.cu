@@ -14,17 +14,13 @@
 // logits ran out of memory at 22K tokens. Here every score lives only in
 // registers; key tiles stream through a per-query running top-k in shared
 // memory. Scratch is the schedule, at most two partial top-k lists per CTA
-// (when a query tile's context is split across CTAs) and, for fp8 caches or
-// with the Hadamard rotation, the prepared queries.
+// (when a query tile's context is split across CTAs) and one shared
+// threshold per query: O(#SMs x k + Tq), whatever the context length.
 //
 // Kernels, in launch order (all with programmatic dependent launch):
 //   plan    one CTA: query tiles (QT queries of one sequence), a prefix sum
 //           of their key-tile counts, and each CTA's first query tile, so the
 //           CTAs split the total work evenly with one dependent load.
-//   qprep   fp8 caches or Hadamard rotation only: q rotated (if on) and, for
-//           fp8 caches, split into e4m3 terms with a power-of-two scale per
-//           (query, head), the scales folded into the head weights, so the
-//           tensor cores take the stored e4m3 keys as they are.
 //   score   persistent, one CTA per SM, warp-specialised:
 //             warp 0      producer: page-table lookups, TMA of 64-token pages
 //                         (and, for fp8 one-query tiles, a bulk copy of the
@@ -32,7 +28,12 @@
 //             warp 1      MMA issuer: tcgen05.mma M=128 keys x N=QT*64 heads
 //                         x K=128 into a ring of TMEM accumulators (4 for
 //                         one-query tiles, 2 for four-query tiles)
-//             score warps tcgen05.ld, ReLU, head-weighted sum, fp8 key
+//             score warps at the start of a query tile, for fp8 caches or
+//                         the Hadamard rotation: the tile's bf16 query rows
+//                         rotated (if on) and turned into tensor-core terms
+//                         in place (e4m3 terms with a power-of-two scale per
+//                         row, folded into the head weight); then per key
+//                         tile tcgen05.ld, ReLU, head-weighted sum, fp8 key
 //                         scale, mask; one score per key staged in a ring of
 //                         shared-memory slots
 //             top-k groups of 4 warps: threshold filter of the staged scores
@@ -76,7 +77,7 @@ struct PlanHdr {
 // Per query tile: {b, row0, nrows, ntile} and {L, qpos0, 0, 0} where qpos0 is
 // the position of the tile's first query.
 struct WsLayout {
-  size_t hdr, meta, prefix, counters, rec, partials, gthr, qh, wq, total;
+  size_t hdr, meta, prefix, counters, rec, partials, gthr, total;
   int QT, G, qtmax, NG;
 };
 
@@ -89,15 +90,10 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline int pick_qt(int Tq, int B, bool hadamard) {
   return (!hadamard && Tq >= 2 * B && Tq >= 4) ? 4 : 1;
 }
-// Terms the query is carried in: bf16 caches 1 (2 with the rotation: hi and
-// lo), fp8 caches 2 e4m3 terms (3 with the rotation).
-inline int query_terms(int fmt, bool hadamard) {
-  return fmt == DSA_FMT_BF16 ? (hadamard ? 2 : 1) : (hadamard ? 3 : 2);
-}
 // selection size (the sorting networks' K) for an output of k entries
 inline int select_size(int k) { return k <= 512 ? 512 : 1024; }
 
-WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
+WsLayout ws_layout(int num_sms, int Tq, int B, int k, bool hadamard) {
   WsLayout L{};
   L.QT = pick_qt(Tq, B, hadamard);
   L.NG = L.QT;  // top-k groups (one per query): merge counters per (query tile, group)
@@ -118,13 +114,6 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, int fmt, bool hadamard) {
   o = up256(o + static_cast<size_t>(2) * L.G * L.QT * k * 8);
   L.gthr = o;  // per query row: the largest running k-th key published by its pieces
   o = up256(o + static_cast<size_t>(Tq) * 8);
-  if (fmt == DSA_FMT_FP8 || hadamard) {  // prepared queries (all terms) and head weights
-    L.qh = o;
-    const size_t bytes_per_value = static_cast<size_t>(query_terms(fmt, hadamard)) * (fmt == DSA_FMT_BF16 ? 2 : 1);
-    o = up256(o + static_cast<size_t>(Tq) * kH * kD * bytes_per_value);
-    L.wq = o;
-    o = up256(o + static_cast<size_t>(Tq) * kH * 4);
-  }
   L.total = o;
   return L;
 }
@@ -313,41 +302,42 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 }
 
 // ------------------------------------------------------------------ query preparation
-// Fp8 key tiles go to the tensor cores as they are stored (kind::f8f6f4,
-// e4m3 x e4m3, both operands of one type), so each query row is split into
-// e4m3 terms whose sum is the query: one warp per (query, head) row of 128
-// values; a power-of-two scale 2^e puts the row's largest magnitude in
-// [2^7, 2^8); t1 = e4m3(2^e q), t2 = e4m3(2^e q - t1), t3 = e4m3(... - t2),
-// each difference exact in fp32. A bf16 value has 8 significant bits and an
-// e4m3 normal 4, so two terms give 2^e q exactly whenever the remainder is
-// not below e4m3's subnormal step, i.e. for every value at least 2^-10 of
-// the row's maximum; smaller ones keep an absolute error of at most 2^-10
-// (scaled units). Products of e4m3 operands are exact in the fp32
-// accumulator, and w' = w * 2^-e undoes the scale after the ReLU
-// (relu(2^e x) = 2^e relu(x)).
+// The query tile arrives in shared memory as the caller's bf16 rows (two
+// 64-column halves of N rows, 128-byte swizzle). Where it is not used as it
+// is, one warp turns a (query, head) row of 128 values into its tensor-core
+// terms in place, each lane taking 4 consecutive values:
+//
+// fp8 caches: the stored e4m3 keys go to the tensor cores as they are
+// (kind::f8f6f4, e4m3 x e4m3, both operands of one type), so the row is
+// split into e4m3 terms whose sum is the query: a power-of-two scale 2^e
+// puts the row's largest magnitude in [2^7, 2^8); t1 = e4m3(2^e q),
+// t2 = e4m3(2^e q - t1) (t3 likewise), each difference exact in fp32. A
+// bf16 value has 8 significant bits and an e4m3 normal 4, so two terms give
+// 2^e q exactly whenever the remainder is not below e4m3's subnormal step,
+// i.e. for every value at least 2^-10 of the row's maximum; smaller ones
+// keep an absolute error of at most 2^-10 (scaled units). Products of e4m3
+// operands are exact in the fp32 accumulator, and the row's head weight
+// w' = w * 2^-e undoes the scale after the ReLU (relu(2^e x) = 2^e relu(x)).
 //
 // With the Hadamard rotation on, the row is first rotated by the same
 // unnormalised Walsh-Hadamard transform as the stored keys (fp32 butterflies
 // in the store's order: h = 1, 2 inside a lane's 4 values, h = 4 .. 64
 // between lanes l and l ^ (h/4)); the rotated values are sums of up to 128
 // bf16 values and carry more bits than one bf16 or two e4m3 terms hold, so
-// they are kept as NQ terms: bf16 caches take hi = bf16(x) and
-// lo = bf16(x - hi) (16 significant bits), fp8 caches three e4m3 terms
-// (12 significant bits). w' carries a further 2^-7 (the transform's gain 128
-// on the dot product).
-// Output: term 0 rows, then term 1 rows, ... (each term [rows][128] bf16 or
-// e4m3), and w'.
-template <bool E4M3, bool HAD>
-__global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
-                                                    const float* __restrict__ w,
-                                                    uint32_t* __restrict__ qe, float* __restrict__ wq,
-                                                    long long rows) {
-  pdl_wait();
-  pdl_trigger();
-  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const uint2 v = q[r * 32 + lane];
+// bf16 caches take hi = bf16(x) and lo = bf16(x - hi) (16 significant bits)
+// and fp8 caches three e4m3 terms (12 significant bits); w' carries a
+// further 2^-7 (the transform's gain 128 on the dot product).
+//
+// Terms follow one another in shared memory: a bf16 term as two 64-column
+// halves, an e4m3 term as one 128-byte row, all of N rows. The first two
+// e4m3 terms of row r, and the hi term, take the same two 128-byte lines as
+// the row's bf16 values, so a warp converts its row in place once every
+// lane has read it.
+template <bool E4M3, bool HAD, int N, int NQ>
+__device__ __forceinline__ void prep_row(uint8_t* sQ, int r, float* sw, int lane) {
+  const int half = lane >> 4, chunk = (lane & 15) >> 1;  // values 4l..4l+3
+  const int in_off = r * 128 + ((chunk ^ (r & 7)) << 4) + (lane & 1) * 8;
+  const uint2 v = *reinterpret_cast<const uint2*>(sQ + half * (N * 128) + in_off);
   float x[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
                 __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)};
   if constexpr (HAD) {
@@ -373,49 +363,50 @@ __global__ void __launch_bounds__(256) qprep_kernel(const uint2* __restrict__ q,
   }
   constexpr int kGain = HAD ? 7 : 0;  // log2 of the rotation's gain on q . k
   if constexpr (!E4M3) {
-    // bf16 caches (only with the rotation): hi and lo bf16 terms
+    // bf16 caches (only with the rotation): hi in place, lo as the next term
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]);
+    const __nv_bfloat162 h1 = __floats2bfloat162_rn(x[2], x[3]);
+    const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(__fsub_rn(x[0], f0.x), __fsub_rn(x[1], f0.y));
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(__fsub_rn(x[2], f1.x), __fsub_rn(x[3], f1.y));
     uint2 hi2, lo2;
-    {
-      const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]);
-      const __nv_bfloat162 h1 = __floats2bfloat162_rn(x[2], x[3]);
-      const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-      const __nv_bfloat162 l0 = __floats2bfloat162_rn(__fsub_rn(x[0], f0.x), __fsub_rn(x[1], f0.y));
-      const __nv_bfloat162 l1 = __floats2bfloat162_rn(__fsub_rn(x[2], f1.x), __fsub_rn(x[3], f1.y));
-      hi2.x = *reinterpret_cast<const uint32_t*>(&h0);
-      hi2.y = *reinterpret_cast<const uint32_t*>(&h1);
-      lo2.x = *reinterpret_cast<const uint32_t*>(&l0);
-      lo2.y = *reinterpret_cast<const uint32_t*>(&l1);
-    }
-    reinterpret_cast<uint2*>(qe)[r * 32 + lane] = hi2;
-    reinterpret_cast<uint2*>(qe)[(rows + r) * 32 + lane] = lo2;
-    if (lane == 0) wq[r] = ldexpf(w[r], -kGain);
+    hi2.x = *reinterpret_cast<const uint32_t*>(&h0);
+    hi2.y = *reinterpret_cast<const uint32_t*>(&h1);
+    lo2.x = *reinterpret_cast<const uint32_t*>(&l0);
+    lo2.y = *reinterpret_cast<const uint32_t*>(&l1);
+    __syncwarp();
+    *reinterpret_cast<uint2*>(sQ + half * (N * 128) + in_off) = hi2;
+    *reinterpret_cast<uint2*>(sQ + 2 * (N * 128) + half * (N * 128) + in_off) = lo2;
+    if (lane == 0) sw[r] = sw[r] * (1.0f / (1 << kGain));
   } else {
-    constexpr int NQ = HAD ? 3 : 2;
     float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    int e = 0;
-    if (m > 0.f) {
-      int ex;
-      frexpf(m, &ex);  // m = f * 2^ex, f in [0.5, 1)
-      e = 8 - ex;
-    }
+    // e such that m * 2^e lies in [2^7, 2^8): from m's exponent field (a
+    // subnormal or zero row takes the largest e kept normal, 126); both 2^e
+    // and 2^-e are exact fp32 powers of two built from their bits
+    const int be = (__float_as_int(m) >> 23) & 0xFF;
+    const int e = be == 0 ? 126 : min(134 - be, 126);
+    const float up = __int_as_float((127 + e) << 23);
+    const float down = __int_as_float(max(127 - e - kGain, 1) << 23);  // 2^-(e + gain), at least 2^-126
     uint32_t t[NQ] = {};
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-      float y0 = ldexpf(x[2 * p], e), y1 = ldexpf(x[2 * p + 1], e);
+      float y0 = x[2 * p] * up, y1 = x[2 * p + 1] * up;
 #pragma unroll
       for (int term = 0; term < NQ; ++term) {
-        const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
-        t[term] |= static_cast<uint32_t>(a) << (16 * p);
-        const __half2_raw ah = __nv_cvt_fp8x2_to_halfraw2(a, __NV_E4M3);
-        y0 = __fsub_rn(y0, __half2float(__ushort_as_half(ah.x)));  // exact: the remainder
-        y1 = __fsub_rn(y1, __half2float(__ushort_as_half(ah.y)));
+        const __nv_fp8x2_storage_t q2 = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+        t[term] |= static_cast<uint32_t>(q2) << (16 * p);
+        const __half2_raw qh = __nv_cvt_fp8x2_to_halfraw2(q2, __NV_E4M3);
+        y0 = __fsub_rn(y0, __half2float(__ushort_as_half(qh.x)));  // exact: the remainder
+        y1 = __fsub_rn(y1, __half2float(__ushort_as_half(qh.y)));
       }
     }
+    __syncwarp();  // the row's bf16 values are read by every lane before the terms replace them
+    const int out_off = r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + (lane & 3) * 4;
 #pragma unroll
-    for (int term = 0; term < NQ; ++term) qe[(term * rows + r) * 32 + lane] = t[term];
-    if (lane == 0) wq[r] = ldexpf(w[r], -e - kGain);
+    for (int term = 0; term < NQ; ++term) *reinterpret_cast<uint32_t*>(sQ + term * (N * 128) + out_off) = t[term];
+    if (lane == 0) sw[r] = sw[r] * down;
   }
 }
 
@@ -456,6 +447,12 @@ struct Cfg {
   static constexpr int TMEM_COLS = NTB * N;
   static constexpr int TERM_BYTES = N * 128 * (FMT == DSA_FMT_BF16 ? 2 : 1);  // one query term
   static constexpr int Q_BYTES = NQ * TERM_BYTES;
+  // the query tile arrives as the caller's bf16 rows (N x 256 bytes) and,
+  // unless it is used as it is (bf16 cache, no rotation), the score warps
+  // turn it into its terms in place
+  static constexpr bool PREP = FMT == DSA_FMT_FP8 || NQ > 1;
+  static constexpr bool HAD = FMT == DSA_FMT_BF16 ? NQ == 2 : NQ == 3;
+  static_assert(!HAD || PREP, "the rotation is applied by the conversion");
   static constexpr int OP_BYTES = kTile * (FMT == DSA_FMT_BF16 ? 256 : 128);
   static constexpr int ST_BYTES = QT * kTile * 4;        // one staged tile of scores
   static constexpr int OFF_Q = 0;
@@ -484,6 +481,7 @@ struct Misc {
   uint64_t tm_full[4], tm_empty[4], q_full, q_empty, fin, w_full[2], w_empty[2];
   uint64_t st_full[16], st_empty[16];
   uint64_t sc_full[16], sc_empty[16];
+  uint64_t prep[2];  // the query tile of a weight buffer has been turned into its terms
   uint32_t tmem_base;
   int abort;
   int cnt[4];
@@ -501,7 +499,7 @@ struct ScoreArgs {
   const uint8_t* cache;
   int num_pages;
   const float* w;  // head weights (prepared queries: with their scales folded in)
-  long long qrows;  // (query, head) rows; each further query term's rows follow
+  long long qrows;  // (query, head) rows
   const char* ws;
   WsLayout L;
   int32_t* out_idx;
@@ -936,6 +934,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ms->w_full[i], 1);
       mbar_init(&ms->w_empty[i], C::NSW);
+      mbar_init(&ms->prep[i], C::NSW);
     }
     mbar_init(&ms->fin, 1);
     ms->abort = 0;
@@ -990,18 +989,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           atomicOr(a.status, DSA_DEV_TIMEOUT);
           *abort_flag = 1;
         } else {
-          mbar_arrive_expect_tx(&ms->q_full, C::Q_BYTES);
-#pragma unroll
-          for (int term = 0; term < NQ; ++term) {
-            const int y = static_cast<int>(term * a.qrows) + s.row0 * kH;
-            uint8_t* dq = sQ + term * C::TERM_BYTES;
-            if constexpr (FMT == DSA_FMT_BF16) {  // two 64-column halves
-              tma_load_2d(dq, &tm_q, 0, y, &ms->q_full);
-              tma_load_2d(dq + C::N * 128, &tm_q, 64, y, &ms->q_full);
-            } else {  // one 128-byte row per (query, head)
-              tma_load_2d(dq, &tm_q, 0, y, &ms->q_full);
-            }
-          }
+          // the caller's bf16 rows, as two 64-column halves
+          mbar_arrive_expect_tx(&ms->q_full, C::N * 256);
+          tma_load_2d(sQ, &tm_q, 0, s.row0 * kH, &ms->q_full);
+          tma_load_2d(sQ + C::N * 128, &tm_q, 64, s.row0 * kH, &ms->q_full);
         }
         // the tile's head-weight rows into the weight buffer the epilogue
         // released two query tiles ago (each buffer has its own barriers, so
@@ -1106,7 +1097,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
       Seg s;
       bool stop = false;
       while (!stop && it.next(s)) {
-        if (!mbar_wait(&ms->q_full, seg_i & 1)) {
+        const bool qok = C::PREP ? mbar_wait(&ms->prep[seg_i & 1], (seg_i >> 1) & 1)
+                                 : mbar_wait(&ms->q_full, seg_i & 1);
+        if (!qok) {
           atomicOr(a.status, DSA_DEV_TIMEOUT);
           *abort_flag = 1;
           break;
@@ -1168,12 +1161,32 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     bool stop = false;
     while (!stop && it.next(s)) {
       const int32_t* pt = a.page_table + static_cast<long long>(s.b) * a.max_pages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&ms->w_full[seg_i & 1], (seg_i >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ms->w_full[seg_i & 1], (seg_i >> 1) & 1) &&
+                                       (!C::PREP || mbar_wait(&ms->q_full, seg_i & 1)))) {
         if (lane == 0) {
           atomicOr(a.status, DSA_DEV_TIMEOUT);
           *abort_flag = 1;
         }
         break;
+      }
+      if constexpr (C::PREP) {
+        // this warp's rows of the query tile into their terms (and the rows'
+        // head weights rescaled), then wait until every row is done: the MMA
+        // needs all of them and this warp reads every head weight of its
+        // queries
+        float* sWp = sW + (seg_i & 1) * (QT * 64);
+        for (int r = warp - C::W_SCORE; r < C::N; r += C::NSW)
+          prep_row<FMT == DSA_FMT_FP8, C::HAD, C::N, NQ>(sQ, r, sWp, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms->prep[seg_i & 1]);
+        if (!__all_sync(0xffffffffu, mbar_wait(&ms->prep[seg_i & 1], (seg_i >> 1) & 1))) {
+          if (lane == 0) {
+            atomicOr(a.status, DSA_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+          break;
+        }
       }
       const float* sWs = sW + (seg_i & 1) * (QT * 64);
       const int ring = C::ALT ? (seg_i & 1) : 0;
@@ -1498,7 +1511,8 @@ dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtenso
 int max_sequences() { return kMaxSeqs; }
 
 size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt) {
-  return ws_layout(ctx->num_sms, Tq, B, select_size(k), fmt, ctx->hadamard != 0).total;
+  (void)fmt;  // the same for both cache formats
+  return ws_layout(ctx->num_sms, Tq, B, select_size(k), ctx->hadamard != 0).total;
 }
 
 dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const void* cache,
@@ -1507,14 +1521,13 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
                        int32_t B, int32_t Tq, int32_t causal, int32_t k, int32_t* out_idx,
                        float* out_score, void* workspace, size_t ws_bytes, cudaStream_t stream) {
   (void)ws_bytes;
-  // tensor-map row coordinates are 32-bit: the (query, head) rows of every
-  // query term must stay below 2^31
-  if (static_cast<long long>(Tq) * kH * query_terms(fmt, ctx->hadamard != 0) > 0x7FFFFFFFLL)
-    return DSA_ERR_UNSUPPORTED;
+  // tensor-map row coordinates are 32-bit: the (query, head) rows must stay
+  // below 2^31
+  if (static_cast<long long>(Tq) * kH > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
   // any k <= 1024 runs the top-512 or top-1024 selection and writes the
   // first k entries of each sorted row
   const int ksel = select_size(k);
-  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, ksel, fmt, ctx->hadamard != 0);
+  const WsLayout L = ws_layout(ctx->num_sms, Tq, B, ksel, ctx->hadamard != 0);
   char* ws = static_cast<char*>(workspace);
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
@@ -1528,41 +1541,16 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
       return DSA_ERR_CUDA;
   }
 
-  const void* qsrc = q;
-  const float* wsrc = head_w;
   const long long rows = static_cast<long long>(Tq) * kH;
-  if (fmt == DSA_FMT_FP8 || ctx->hadamard) {
-    const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
-    LaunchScope scope(ctx, DSA_K_QPREP, stream);
-    const bool e4 = fmt == DSA_FMT_FP8;
-    auto kern = ctx->hadamard ? (e4 ? qprep_kernel<true, true> : qprep_kernel<false, true>)
-                              : qprep_kernel<true, false>;
-    if (launch_pdl(kern, dim3(blocks), dim3(256), 0, stream, static_cast<const uint2*>(q),
-                   head_w, reinterpret_cast<uint32_t*>(ws + L.qh), reinterpret_cast<float*>(ws + L.wq),
-                   rows) != cudaSuccess)
-      return DSA_ERR_CUDA;
-    qsrc = ws + L.qh;
-    wsrc = reinterpret_cast<const float*>(ws + L.wq);
-  }
 
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(ctx->encode_tiled);
   CUtensorMap tq, tk;
-  const int nq = query_terms(fmt, ctx->hadamard != 0);
-  if (fmt == DSA_FMT_BF16) {  // [nq * rows x 128] bf16 (the terms one after the other), boxes of 64 columns
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(nq * rows)};
+  {  // the caller's queries: [rows x 128] bf16, boxes of 64 columns x the tile's rows
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD * 2)};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(64 * L.QT)};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qsrc), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return DSA_ERR_CUDA;
-  } else {  // [nq * rows x 128] e4m3: first terms, then second terms, ...
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(nq * rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
-    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(64 * L.QT)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qsrc), dims, strides, box, estr,
+    if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return DSA_ERR_CUDA;
@@ -1594,7 +1582,7 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   args.qrows = rows;
   args.cache = static_cast<const uint8_t*>(cache);
   args.num_pages = num_pages;
-  args.w = wsrc;
+  args.w = head_w;
   args.ws = ws;
   args.L = L;
   args.out_idx = out_idx;

@@ -13,7 +13,7 @@ import os
 
 FMT_BF16 = 0
 FMT_FP8 = 1
-KERNEL_KINDS = ("store", "plan", "qprep", "score_bf16", "score_fp8")
+KERNEL_KINDS = ("store", "plan", "score_bf16", "score_fp8")
 HEADS = 64
 HEAD_DIM = 128
 PAGE_SIZE = 64

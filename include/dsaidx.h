@@ -143,8 +143,10 @@ dsa_status dsa_ctx_set_slot_output(dsa_ctx* ctx, int32_t on);
 
 /* Upper bound of the workspace bytes dsa_index_topk needs for these sizes.
  * It does not grow with the context length: it holds the schedule
- * (O(Tq + B)), split-context partial lists (O(#SMs * k)) and, for fp8
- * caches or with the Hadamard rotation on, the prepared queries (O(Tq)). */
+ * (O(Tq + B)), split-context partial lists (O(#SMs * k)) and one shared
+ * threshold per query (8 bytes). The same for both cache formats: the
+ * queries are turned into their tensor-core terms inside the scorer, in
+ * shared memory. */
 size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k,
                                      dsa_fmt fmt);
 
@@ -197,11 +199,9 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
  * race. Nothing in it needs clearing; each call rewrites what must start at
  * zero. Returns DSA_ERR_WORKSPACE, without launching anything, when
  * dsa_index_topk_workspace_size(ctx, Tq, B, k, fmt) exceeds
- * DSA_STATIC_WORKSPACE_BYTES (on a 152-SM GB300 with one sequence: bf16
- * batches up to about 2.0M queries with k <= 512 and 1.7M with k > 512;
- * fp8 batches, and bf16 batches with the Hadamard rotation on, up to about
- * 1700 and 1400 queries, since they keep the prepared queries, 16.6 KB
- * each, in the scratch). */
+ * DSA_STATIC_WORKSPACE_BYTES (on a 152-SM GB300 with one sequence: batches
+ * up to about 1.29M queries with k <= 512 and 1.07M with k > 512, either
+ * cache format; with the Hadamard rotation on, about 620K and 597K). */
 #define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
 dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_w,
                                  const void* cache, int32_t num_pages, dsa_fmt fmt,
@@ -219,10 +219,9 @@ dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_
 typedef enum {
   DSA_K_STORE = 0,      /* dsa_index_store */
   DSA_K_PLAN = 1,       /* dsa_index_topk: schedule */
-  DSA_K_QPREP = 2,      /* dsa_index_topk, fp8 or Hadamard: query preparation */
-  DSA_K_SCORE_BF16 = 3, /* dsa_index_topk: tensor-core scorer + running top-k, bf16 cache */
-  DSA_K_SCORE_FP8 = 4,  /* the same, fp8 cache */
-  DSA_K_COUNT = 5
+  DSA_K_SCORE_BF16 = 2, /* dsa_index_topk: tensor-core scorer + running top-k, bf16 cache */
+  DSA_K_SCORE_FP8 = 3,  /* the same, fp8 cache */
+  DSA_K_COUNT = 4
 } dsa_kernel_kind;
 dsa_status dsa_profile_enable(dsa_ctx* ctx, int on);
 dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms /* [DSA_K_COUNT] */,

@@ -82,17 +82,42 @@ def test_static_scratch_matches_workspace_path(fmt):
 
 
 def test_static_scratch_rejects_oversized_request():
+    # the smallest batch whose workspace exceeds the fixed array: one
+    # sequence, k = 1024. Every buffer is allocated at its true size (about
+    # 27 GB on the device), so the call could not read outside them even if
+    # it were not refused; it must be refused before anything is launched.
     import torch
     from dsa_sparse_attention_store_gb300 import Context
     ctx = Context(theta=10000.0, eps=1e-6, max_pos=4096)
     try:
-        Tq = 4096   # fp8 keeps 16.6 KB per query in the scratch: more than the fixed array holds
-        wl = I.make_workload("big", [Tq], [Tq], [0], True, 512, seed=43, wid=42)
-        d = U.device_workload(wl, 1, ctx, store_fill=False, store_new=False)
-        out_i = torch.zeros((Tq, 512), dtype=torch.int32, device="cuda")
-        out_s = torch.zeros((Tq, 512), dtype=torch.float32, device="cuda")
-        assert _call_static(ctx, wl, 1, d, 512, out_i, out_s) == 6     # DSA_ERR_WORKSPACE
+        lo, hi = 1, 1 << 22
+        while lo < hi:                                   # largest Tq that fits
+            mid = (lo + hi + 1) // 2
+            if ctx.topk_workspace_size(mid, 1, 1024, 1) <= (32 << 20):
+                lo = mid
+            else:
+                hi = mid - 1
+        Tq = lo + 1
+        assert ctx.topk_workspace_size(Tq, 1, 1024, 1) > (32 << 20)
+        npg = (Tq + 63) // 64
+        d = {
+            "q": torch.empty((Tq, 64, 128), dtype=torch.bfloat16, device="cuda"),
+            "head_w": torch.empty((Tq, 64), dtype=torch.float32, device="cuda"),
+            "cache": torch.zeros(npg * 8448, dtype=torch.uint8, device="cuda"),
+            "page_table": torch.arange(npg, dtype=torch.int32, device="cuda").view(1, npg),
+            "seq_lens": torch.tensor([Tq], dtype=torch.int32, device="cuda"),
+            "cu_q": torch.tensor([0, Tq], dtype=torch.int32, device="cuda"),
+        }
+
+        class W:  # the call's sizes
+            num_pages, max_pages, B, causal = npg, npg, 1, True
+        W.Tq = Tq
+        out_i = torch.zeros((Tq, 1024), dtype=torch.int32, device="cuda")
+        out_s = torch.zeros((Tq, 1024), dtype=torch.float32, device="cuda")
+        assert _call_static(ctx, W, 1, d, 1024, out_i, out_s) == 6     # DSA_ERR_WORKSPACE
         torch.cuda.synchronize()
-        assert int(out_i.abs().sum()) == 0                            # nothing was launched
+        assert int(out_i[:64].abs().sum()) == 0 and int(out_i[-64:].abs().sum()) == 0   # nothing ran
+        del d, out_i, out_s
+        torch.cuda.empty_cache()
     finally:
         ctx.close()
