@@ -58,7 +58,10 @@ __global__ void __launch_bounds__(256) store_kernel(
   float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
   int s = -1;
   if (live) {
-    raw = k_raw[static_cast<long long>(tok) * 16 + l];
+    // the raw keys and the cache writes stream through L2 once (evict-first),
+    // so that the RoPE table rows, shared by every sequence at a position,
+    // stay in L2
+    raw = __ldcs(k_raw + static_cast<long long>(tok) * 16 + l);
     pos = rope_pos[tok];
     s = seq_id[tok];
   }
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(256) store_kernel(
       }
       uint4* dst = reinterpret_cast<uint4*>(cache + static_cast<long long>(page) * (kPage * kD * 2) +
                                             off * (kD * 2)) + l;
-      *dst = make_uint4(w[0], w[1], w[2], w[3]);
+      __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
     }
   } else {
     float amax = 0.f;
@@ -175,8 +178,8 @@ __global__ void __launch_bounds__(256) store_kernel(
         w[v] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
       }
       uint8_t* pg = cache + static_cast<long long>(page) * (kPage * kD + kPage * 4);
-      *reinterpret_cast<uint2*>(pg + off * kD + 8 * l) = make_uint2(w[0], w[1]);
-      if (l == 0) *reinterpret_cast<float*>(pg + kPage * kD + off * 4) = scale;
+      __stcs(reinterpret_cast<uint2*>(pg + off * kD + 8 * l), make_uint2(w[0], w[1]));
+      if (l == 0) __stcs(reinterpret_cast<float*>(pg + kPage * kD + off * 4), scale);
     }
   }
 }

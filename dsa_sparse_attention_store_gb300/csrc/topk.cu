@@ -83,6 +83,8 @@ struct WsLayout {
 
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+constexpr int kMaxGrid = 1024;  // most CTAs of the scorer (one per SM)
+
 // Four-query tiles when the queries outnumber the sequences; one-query tiles
 // for decode and whenever the query carries more than the plain number of
 // terms (the Hadamard rotation), whose larger query tile only fits beside the
@@ -97,7 +99,7 @@ WsLayout ws_layout(int num_sms, int Tq, int B, int k, bool hadamard) {
   WsLayout L{};
   L.QT = pick_qt(Tq, B, hadamard);
   L.NG = L.QT;  // top-k groups (one per query): merge counters per (query tile, group)
-  L.G = num_sms;
+  L.G = std::min(num_sms, kMaxGrid);
   L.qtmax = (Tq + L.QT - 1) / L.QT + B;
   size_t o = 0;
   L.hdr = o;
@@ -191,11 +193,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     const int32_t* __restrict__ cu_q, int B, int Tq,
                                                     int QT, int NG, int causal, int max_pages, int k,
                                                     int ovh, char* ws, WsLayout L, int32_t* out_idx,
-                                                    float* out_score, unsigned int* status) {
+                                                    float* out_score, unsigned int* status, int prefix_in_smem) {
   __shared__ int smi[32];
   __shared__ long long sml[32];
-  extern __shared__ int plan_sm[];
-  int* s_cq = plan_sm;           // [B + 1]
+  __shared__ long long s_rs[kMaxGrid + 1];  // each CTA's range start in the flattened work
+  extern __shared__ long long plan_sm[];
+  long long* s_pre = plan_sm;                                         // [qtmax + 1] when prefix_in_smem
+  int* s_cq = reinterpret_cast<int*>(s_pre + (prefix_in_smem ? L.qtmax + 1 : 0));  // [B + 1]
   int* s_len = s_cq + (B + 1);   // [B]
   int* s_qoff = s_len + B;       // [B + 1]
   pdl_wait();
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     const long long ex = block_excl_scan<long long>(cost, sml, tot);
     if (qt < qtot) {
       prefix[qt] = lcarry + ex;
+      if (prefix_in_smem) s_pre[qt] = lcarry + ex;
       for (int g = 0; g < NG; ++g) cnt[qt * NG + g] = 0;
       for (int r = 0; r < m.z; ++r) gthr[m.y + r] = 0ull;
       if (m.w == 0) {  // no visible keys: the rows are all padding
@@ -278,26 +283,34 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   const int Ge = total < L.G ? static_cast<int>(total) : L.G;
   if (threadIdx.x == 0) {
     prefix[qtot] = total;
+    if (prefix_in_smem) s_pre[qtot] = total;
     hdr->qtot = qtot;
     hdr->Ge = Ge;
     hdr->total = total;
     hdr->ovh = ovh;
   }
+  if (Ge > 0)
+    for (int c = threadIdx.x; c <= Ge; c += 1024) s_rs[c] = range_start(c, total, Ge);
   __syncthreads();
+  // the CTA whose range holds unit u: the last c < Ge with s_rs[c] <= u
+  auto owner = [&](long long u) {
+    int lo = 0, hi = Ge - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_rs[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
   // first query tile of each CTA: the non-empty tile holding its range start;
   // and each query tile's first and last CTA with key tiles of it
   for (int qt = threadIdx.x; qt < qtot; qt += 1024) {
-    const long long p0 = prefix[qt], p1 = prefix[qt + 1];
+    const long long p0 = prefix_in_smem ? s_pre[qt] : prefix[qt];
+    const long long p1 = prefix_in_smem ? s_pre[qt + 1] : prefix[qt + 1];
     if (p1 <= p0) continue;
-    meta[2 * qt + 1].z = owner_of(p0 + ovh, total, Ge);
-    meta[2 * qt + 1].w = owner_of(p1 - 1, total, Ge);
-    int c = static_cast<int>(p0 * Ge / total);
-    while (c > 0 && range_start(c, total, Ge) >= p0) --c;
-    for (; c < Ge; ++c) {
-      const long long st = range_start(c, total, Ge);
-      if (st >= p1) break;
-      if (st >= p0) rec[c] = qt;
-    }
+    meta[2 * qt + 1].z = owner(p0 + ovh);
+    meta[2 * qt + 1].w = owner(p1 - 1);
+    for (int c = owner(p0); c < Ge && s_rs[c] < p1; ++c)
+      if (s_rs[c] >= p0) rec[c] = qt;
   }
 }
 
@@ -1532,12 +1545,16 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
     const int ovh = L.QT == 4 ? 12 : 4;  // measured fixed cost of a query tile, in key tiles
-    const size_t psm = static_cast<size_t>(3 * B + 2) * sizeof(int);
+    // the prefix of the query tiles' costs stays in shared memory when it fits
+    const size_t base = static_cast<size_t>(3 * B + 2) * sizeof(int);
+    const size_t pre = static_cast<size_t>(L.qtmax + 1) * sizeof(long long);
+    const int in_smem = base + pre <= 160 * 1024 ? 1 : 0;
+    const size_t psm = base + (in_smem ? pre : 0);
     if (cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(psm)) != cudaSuccess)
       return DSA_ERR_CUDA;
     if (launch_pdl(plan_kernel, dim3(1), dim3(1024), psm, stream, seq_lens, cu_q, B, Tq, L.QT, L.NG,
-                   causal, max_pages, k, ovh, ws, L, out_idx, out_score, ctx->status) != cudaSuccess)
+                   causal, max_pages, k, ovh, ws, L, out_idx, out_score, ctx->status, in_smem) != cudaSuccess)
       return DSA_ERR_CUDA;
   }
 
