@@ -237,6 +237,24 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   if (threadIdx.x == 0) s_qoff[B] = carry;
   __syncthreads();
   const int qtot = carry;
+  // the merge counters and the shared thresholds start at zero (coalesced)
+  for (int i = threadIdx.x; i < qtot * NG; i += 1024) cnt[i] = 0;
+  for (int i = threadIdx.x; i < Tq; i += 1024) gthr[i] = 0ull;
+  // query tile qt: its sequence b (the last with s_qoff[b] <= qt), index t
+  // in b, first row, rows, first query position
+  auto tile_of = [&](int qt, int& b, int& row0, int& nrows, int& qpos0) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_qoff[mid] <= qt) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    const int t = qt - s_qoff[b];
+    const int q0 = s_cq[b], nq = s_cq[b + 1] - q0;
+    row0 = q0 + t * QT;
+    nrows = min(QT, nq - t * QT);
+    qpos0 = s_len[b] - nq + t * QT;
+  };
 
   long long lcarry = 0;
   for (int base = 0; base < qtot; base += 1024) {
@@ -244,22 +262,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     long long cost = 0;
     int4 m = make_int4(0, 0, 0, 0);
     if (qt < qtot) {
-      int lo = 0, hi = B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_qoff[mid] <= qt) lo = mid; else hi = mid - 1;
-      }
-      const int b = lo;
-      const int t = qt - s_qoff[b];
-      const int q0 = s_cq[b], nq = s_cq[b + 1] - q0, Ls = s_len[b];
-      const int row0 = q0 + t * QT;
-      const int nrows = min(QT, nq - t * QT);
-      const int qpos0 = Ls - nq + t * QT;
-      const int kend = causal ? (qpos0 + nrows) : Ls;
+      int b, row0, nrows, qpos0;
+      tile_of(qt, b, row0, nrows, qpos0);
+      const int kend = causal ? (qpos0 + nrows) : s_len[b];
       const int ntile = kend > 0 ? (kend + kTile - 1) / kTile : 0;
       m = make_int4(b, row0, nrows, ntile);
       meta[2 * qt] = m;
-      meta[2 * qt + 1] = make_int4(Ls, qpos0, 0, 0);
       cost = ntile > 0 ? ntile + ovh : 0;
     }
     long long tot;
@@ -267,8 +275,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     if (qt < qtot) {
       prefix[qt] = lcarry + ex;
       if (prefix_in_smem) s_pre[qt] = lcarry + ex;
-      for (int g = 0; g < NG; ++g) cnt[qt * NG + g] = 0;
-      for (int r = 0; r < m.z; ++r) gthr[m.y + r] = 0ull;
       if (m.w == 0) {  // no visible keys: the rows are all padding
         for (int r = 0; r < m.z; ++r)
           for (int i = 0; i < k; ++i) {
@@ -306,9 +312,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   for (int qt = threadIdx.x; qt < qtot; qt += 1024) {
     const long long p0 = prefix_in_smem ? s_pre[qt] : prefix[qt];
     const long long p1 = prefix_in_smem ? s_pre[qt + 1] : prefix[qt + 1];
-    if (p1 <= p0) continue;
-    meta[2 * qt + 1].z = owner(p0 + ovh);
-    meta[2 * qt + 1].w = owner(p1 - 1);
+    int b, row0, nrows, qpos0;
+    tile_of(qt, b, row0, nrows, qpos0);
+    const bool work = p1 > p0;
+    meta[2 * qt + 1] = make_int4(s_len[b], qpos0, work ? owner(p0 + ovh) : -1, work ? owner(p1 - 1) : -1);
+    if (!work) continue;
     for (int c = owner(p0); c < Ge && s_rs[c] < p1; ++c)
       if (s_rs[c] >= p0) rec[c] = qt;
   }
