@@ -30,13 +30,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  // no suspend-time hint: with a long hint a waiting warp was seen to stay
-  // suspended for microseconds after the phase had completed
+  // the suspend-time hint (ns) lets a waiting thread sleep until the phase
+  // completes instead of re-polling, which leaves the issue slots to the
+  // warps that have work (without it, waiting warps cost the prefill scorer
+  // a large share of its instruction issue)
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }

@@ -446,7 +446,10 @@ struct Cfg {
   static constexpr int NBUF = ALT ? 2 : QT;              // running top-k buffers
   // key-tile operand stages (32 KB bf16, 16 KB e4m3): enough bytes in flight
   // per SM to cover the HBM latency of a streaming one-query tile
-  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? 3 : 6) : (FMT == DSA_FMT_BF16 ? 4 : 6);
+  // (four-query tiles selecting 1024 keys trade a stage for a candidate
+  // buffer twice the selection: a smaller buffer would select every tile)
+  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? (KSEL > 512 ? 2 : 3) : (KSEL > 512 ? 4 : 6))
+                                   : (FMT == DSA_FMT_BF16 ? 4 : 6);
   static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
   // alternating groups each read their own ring of staging slots: a group
   // that skips the other's query tile must not wait on a slot phase that
@@ -456,7 +459,7 @@ struct Cfg {
   // candidate keys of one query's running top-k, cut back to KSEL by radix
   // select when full: one-query tiles get a buffer large enough that a
   // CTA's piece of a decode query usually needs one selection, at its end
-  static constexpr int TK = ALT ? (FMT == DSA_FMT_BF16 && NQ == 2 ? 3072 : 4096) : 1280;
+  static constexpr int TK = ALT ? (FMT == DSA_FMT_BF16 && NQ == 2 ? 3072 : 4096) : (KSEL > 512 ? 2304 : 1280);
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
   static constexpr int NWARPS = W_TOPK + 4 * NTK;
