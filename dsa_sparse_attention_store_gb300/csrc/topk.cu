@@ -513,6 +513,7 @@ struct Misc {
   int gok[4], glast[4], gdigit[4], gabove[4], gcd[4];  // per top-k group
   int wsum[4][2][4];
   unsigned long long gmin[4][4], gmax[4][4];
+  unsigned int hmax[4];  // per buffer: largest score word pushed in the query tile
 };
 static_assert(sizeof(Misc) <= 2048, "misc");
 
@@ -771,6 +772,108 @@ __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, 
     *thr = prefix > 0 ? prefix - 1 : 0;
   }
   named_bar(barid, 128);
+}
+
+// Cut buf[0..n) back, cheaply, to the keys of the top score bins holding at
+// least K keys, once a threshold is known: every key lies above the current
+// threshold, so the high words (ordered scores) span thr_hi .. hmax; 256
+// bins of a power-of-two width cover that span, one histogram finds the bin
+// B that holds the K-th largest key, and the keys of bins >= B stay: K ..
+// K + |B| of them. The threshold rises to just below bin B's lower edge,
+// which is at most the K-th largest key, so no key of the top K is lost.
+// Two passes over the buffer (histogram, compaction) where the exact radix
+// select takes six to eight. Returns false, leaving the buffer as it is,
+// when the cut would keep more than `room` keys. hist: 256 words.
+__device__ bool group_cut(uint64_t* buf, int* cnt, unsigned long long* thr, unsigned int hmax, int K,
+                          int room, uint32_t* hist, Misc* ms, int g, int gt, int barid) {
+  const int n = *cnt;
+  if (n <= K) return true;
+  const int w = gt >> 5, lane = gt & 31;
+  const uint32_t lo = static_cast<uint32_t>(*thr >> 32);
+  if (hmax < lo) return false;
+  const uint64_t span1 = static_cast<uint64_t>(hmax - lo);  // span - 1
+  const int sh = span1 >= 256 ? (64 - __clzll(static_cast<long long>(span1))) - 8 : 0;
+  for (int i = gt; i < 256; i += 128) hist[i] = 0u;
+  named_bar(barid, 128);
+  for (int i = gt; i < n; i += 128) {
+    const uint32_t h = static_cast<uint32_t>(buf[i] >> 32);
+    atomicAdd(&hist[(h - lo) >> sh], 1u);
+  }
+  named_bar(barid, 128);
+  if (gt < 32) {
+    // lane l holds bins 255-8l .. 248-8l (descending)
+    int c[8], sum = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = static_cast<int>(hist[255 - 8 * gt - e]);
+      sum += c[e];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (gt >= o) incl += y;
+    }
+    const int excl = incl - sum;
+    if (excl < K && K <= incl) {
+      int acc = excl;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc += c[e];
+        if (acc >= K) {
+          ms->gdigit[g] = 255 - 8 * gt - e;  // bin B
+          ms->gabove[g] = acc;               // keys kept
+          break;
+        }
+      }
+    }
+  }
+  named_bar(barid, 128);
+  const int B = ms->gdigit[g];
+  const int kept = ms->gabove[g];
+  if (kept > room) return false;
+  const uint32_t edge = lo + (static_cast<uint32_t>(B) << sh);
+  int base = 0;
+  for (int r0 = 0; r0 < n; r0 += 512) {
+    uint64_t kv[4];
+    int keep = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = r0 + e * 128 + gt;
+      kv[e] = i < n ? buf[i] : 0ull;
+      keep += (i < n && static_cast<uint32_t>(kv[e] >> 32) >= edge) ? 1 : 0;
+    }
+    int incl = keep;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int par = (r0 >> 9) & 1;
+    if (lane == 31) ms->wsum[g][par][w] = incl;
+    named_bar(barid, 128);
+    int off = base + incl - keep, tot = 0;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int v = ms->wsum[g][par][x];
+      if (x < w) off += v;
+      tot += v;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = r0 + e * 128 + gt;
+      if (i < n && static_cast<uint32_t>(kv[e] >> 32) >= edge) buf[off++] = kv[e];
+    }
+    base += tot;
+  }
+  named_bar(barid, 128);
+  if (gt == 0) {
+    *cnt = base;
+    const unsigned long long t = (static_cast<unsigned long long>(edge) << 32) - 1ull;
+    if (t > *thr) *thr = t;
+  }
+  named_bar(barid, 128);
+  return true;
 }
 
 // Compare-exchange of registers e and e ^ S (stride S < E) of each thread;
@@ -1376,6 +1479,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
         if (gt == 0) {
           ms->cnt[jb] = 0;
           ms->thr[jb] = 0;
+          ms->hmax[jb] = 0u;
         }
         thr[jj] = 0;
         nsel[jj] = 0;
@@ -1395,6 +1499,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
             const uint64_t key = make_key(sc, pos);
             const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
             push_key(pass, key, qlist(jj), &ms->cnt[jb], lane);
+            const unsigned int hw = __reduce_max_sync(0xffffffffu, pass ? static_cast<unsigned int>(key >> 32) : 0u);
+            if (lane == 0 && hw) atomicMax(&ms->hmax[jb], hw);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->st_empty[st]);
@@ -1417,7 +1523,11 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           // piece's last selection) small
           const int limit = (C::ALT && nsel[jj] == 0) ? 2 * KSEL : C::TK;
           if (ms->cnt[jb] > limit - kTile) {
-            group_compact(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+            // after the first (exact) selection the threshold bounds the
+            // scores from below and the cheap cut usually suffices
+            if (nsel[jj] == 0 || !group_cut(qlist(jj), &ms->cnt[jb], &ms->thr[jb], ms->hmax[jb], KSEL,
+                                            limit - 2 * kTile, hist, ms, tg, gt, barid))
+              group_compact(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
             ++nsel[jj];
             unsigned long long t_new = ms->thr[jb];
             const int j = qrow(jj);
