@@ -224,7 +224,7 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
 
 size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k,
                                      dsa_fmt fmt) {
-  if (!ctx || Tq < 0 || B <= 0 || k < 1 || k > 1024) return 0;
+  if (!ctx || Tq < 0 || B <= 0 || k < 1 || k > 2048) return 0;
   if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return 0;
   return dsa::topk_workspace(ctx, Tq, B, k, fmt);
 }
@@ -237,7 +237,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
                           dsa_stream_t stream) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
   if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return DSA_ERR_UNSUPPORTED;
-  if (k < 1 || k > 1024) return DSA_ERR_UNSUPPORTED;
+  if (k < 1 || k > 2048) return DSA_ERR_UNSUPPORTED;
   if (Tq < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(num_pages) * 64 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
   if (B > dsa::max_sequences()) return DSA_ERR_UNSUPPORTED;

@@ -86,18 +86,19 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 constexpr int kMaxGrid = 1024;  // most CTAs of the scorer (one per SM)
 
 // Four-query tiles when the queries outnumber the sequences; one-query tiles
-// for decode and whenever the query carries more than the plain number of
-// terms (the Hadamard rotation), whose larger query tile only fits beside the
-// operand ring of a one-query tile.
-inline int pick_qt(int Tq, int B, bool hadamard) {
-  return (!hadamard && Tq >= 2 * B && Tq >= 4) ? 4 : 1;
+// for decode, whenever the query carries more than the plain number of terms
+// (the Hadamard rotation), whose larger query tile only fits beside the
+// operand ring of a one-query tile, and for selections of 2048 keys, whose
+// candidate buffer only fits there.
+inline int pick_qt(int Tq, int B, bool hadamard, int ksel) {
+  return (!hadamard && ksel <= 1024 && Tq >= 2 * B && Tq >= 4) ? 4 : 1;
 }
 // selection size (the sorting networks' K) for an output of k entries
-inline int select_size(int k) { return k <= 512 ? 512 : 1024; }
+inline int select_size(int k) { return k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048); }
 
 WsLayout ws_layout(int num_sms, int Tq, int B, int k, bool hadamard) {
   WsLayout L{};
-  L.QT = pick_qt(Tq, B, hadamard);
+  L.QT = pick_qt(Tq, B, hadamard, k);
   L.NG = L.QT;  // top-k groups (one per query): merge counters per (query tile, group)
   L.G = std::min(num_sms, kMaxGrid);
   L.qtmax = (Tq + L.QT - 1) / L.QT + B;
@@ -460,6 +461,9 @@ struct Cfg {
   // select when full: one-query tiles get a buffer large enough that a
   // CTA's piece of a decode query usually needs one selection, at its end
   static constexpr int TK = ALT ? (FMT == DSA_FMT_BF16 && NQ == 2 ? 3072 : 4096) : (KSEL > 512 ? 2304 : 1280);
+  // a selection keeps KSEL keys and the cut aims below TK - 2 tiles: both
+  // must leave room for at least one more tile
+  static_assert(TK >= KSEL + 2 * 128 + 128, "candidate buffer too small for the selection");
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
   static constexpr int NWARPS = W_TOPK + 4 * NTK;
@@ -930,6 +934,8 @@ __device__ __forceinline__ void net_stage(uint64_t (&v)[K / 128], int size, int 
     if constexpr (E > 1) if (stride == 1) net_reg_stage<K, 1>(v, size, w, lane);
     if constexpr (E > 2) if (stride == 2) net_reg_stage<K, 2>(v, size, w, lane);
     if constexpr (E > 4) if (stride == 4) net_reg_stage<K, 4>(v, size, w, lane);
+    if constexpr (E > 8) if (stride == 8) net_reg_stage<K, 8>(v, size, w, lane);
+    static_assert(E <= 16, "register strides above 8");
   }
 }
 
@@ -1521,7 +1527,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           // first selection of a one-query tile comes at 2 KSEL candidates,
           // early enough that its threshold keeps the buffer (and the
           // piece's last selection) small
-          const int limit = (C::ALT && nsel[jj] == 0) ? 2 * KSEL : C::TK;
+          constexpr int kFirst = 2 * KSEL < C::TK ? 2 * KSEL : C::TK;
+          const int limit = (C::ALT && nsel[jj] == 0) ? kFirst : C::TK;
           if (ms->cnt[jb] > limit - kTile) {
             // after the first (exact) selection the threshold bounds the
             // scores from below and the cheap cut usually suffices
@@ -1636,8 +1643,11 @@ dsa_status run_score(dsa_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
 template <int QT, int FMT, int NQ>
 dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtensorMap& tk,
                        const ScoreArgs& args, int G, cudaStream_t stream) {
-  return k == 512 ? run_score<QT, FMT, 512, NQ>(ctx, tq, tk, args, G, stream)
-                  : run_score<QT, FMT, 1024, NQ>(ctx, tq, tk, args, G, stream);
+  if (k == 512) return run_score<QT, FMT, 512, NQ>(ctx, tq, tk, args, G, stream);
+  if constexpr (QT == 1) {  // 2048-key selections run in one-query tiles only
+    if (k == 2048) return run_score<QT, FMT, 2048, NQ>(ctx, tq, tk, args, G, stream);
+  }
+  return run_score<QT, FMT, 1024, NQ>(ctx, tq, tk, args, G, stream);
 }
 
 }  // namespace
@@ -1658,8 +1668,8 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   // tensor-map row coordinates are 32-bit: the (query, head) rows must stay
   // below 2^31
   if (static_cast<long long>(Tq) * kH > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;
-  // any k <= 1024 runs the top-512 or top-1024 selection and writes the
-  // first k entries of each sorted row
+  // any k <= 2048 runs the top-512, top-1024 or top-2048 selection and
+  // writes the first k entries of each sorted row
   const int ksel = select_size(k);
   const WsLayout L = ws_layout(ctx->num_sms, Tq, B, ksel, ctx->hadamard != 0);
   char* ws = static_cast<char*>(workspace);

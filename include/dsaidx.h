@@ -56,7 +56,7 @@ typedef struct CUstream_st* dsa_stream_t; /* a cudaStream_t; NULL = legacy defau
 typedef enum {
   DSA_OK = 0,
   DSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer ... */
-  DSA_ERR_UNSUPPORTED = 2,   /* k not in 1..1024, unknown format, no sm_103 device */
+  DSA_ERR_UNSUPPORTED = 2,   /* k not in 1..2048, unknown format, no sm_103 device */
   DSA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
   DSA_ERR_DEVICE_BOUNDS = 4, /* device saw a page id / position / sequence out of range */
   DSA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
@@ -169,10 +169,12 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  *              page are not read.
  *  seq_lens    (device) [B] int32, n_q(b) <= seq_lens[b] <= 64*max_pages.
  *  cu_q        (device) [B+1] int32, cu_q[0] = 0, non-decreasing, cu_q[B] = Tq.
- *  k           1 .. 1024 (the pages use 512 and 1024; other k run the top-512
- *              or top-1024 selection and keep the first k of each sorted
- *              row).  B <= 16384 and Tq < 2^24 (2^31 / 192 with the Hadamard
- *              rotation on an fp8 cache), else DSA_ERR_UNSUPPORTED.
+ *  k           1 .. 2048 (the pages use 512 and 1024, and a downstream
+ *              gather may take 2048; other k run the top-512, top-1024 or
+ *              top-2048 selection and keep the first k of each sorted row;
+ *              k > 1024 runs in one-query tiles, the decode kernel, whatever
+ *              the batch: a 2048-key candidate buffer only fits there).
+ *              B <= 16384 and Tq < 2^25, else DSA_ERR_UNSUPPORTED.
  *  out_idx     (device) [Tq][k] int32;  out_score (device) [Tq][k] fp32.
  *  workspace   (device) >= dsa_index_topk_workspace_size(...) bytes, 256-byte
  *              aligned; contents need not be initialised and are scratch.
@@ -200,8 +202,9 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
  * zero. Returns DSA_ERR_WORKSPACE, without launching anything, when
  * dsa_index_topk_workspace_size(ctx, Tq, B, k, fmt) exceeds
  * DSA_STATIC_WORKSPACE_BYTES (on a 152-SM GB300 with one sequence: batches
- * up to about 1.29M queries with k <= 512 and 1.07M with k > 512, either
- * cache format; with the Hadamard rotation on, about 620K and 597K). */
+ * up to about 1.29M queries with k <= 512 and 1.07M with 512 < k <= 1024,
+ * either cache format; with the Hadamard rotation on, about 620K and 597K;
+ * with k > 1024, about 549K, rotation on or off). */
 #define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
 dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_w,
                                  const void* cache, int32_t num_pages, dsa_fmt fmt,

@@ -60,8 +60,8 @@ def test_invalid_arguments_rejected_without_device(L):
     # T == 0 is a no-op
     assert L.dsa_index_store(fake, None, None, None, None, 0, 1, 1, None, 1, 0, None) == 0
     args = [good, good, good, 1, 0, good, 1, good, good, 1, 4, 1]
-    # k above 1024
-    assert L.dsa_index_topk(fake, *args, 2048, good, good, good, 1 << 30, None) == 2
+    # k above 2048
+    assert L.dsa_index_topk(fake, *args, 2049, good, good, good, 1 << 30, None) == 2
     assert L.dsa_index_topk(None, *args, 512, good, good, good, 1 << 30, None) == 1
     # unknown format
     bad = list(args)
@@ -79,10 +79,10 @@ def test_invalid_arguments_rejected_without_device(L):
     assert L.dsa_ctx_set_hadamard(None, 1) == 1
     assert L.dsa_ctx_set_slot_output(None, 1) == 1
     assert L.dsa_selftest_bounded_wait(None, None) == 1
-    # k outside 1 .. 1024
+    # k outside 1 .. 2048
     assert L.dsa_index_topk(fake, *args, 0, good, good, good, 1 << 30, None) == 2
-    assert L.dsa_index_topk(fake, *args, 1025, good, good, good, 1 << 30, None) == 2
-    assert L.dsa_index_topk_workspace_size(fake, 4, 1, 1025, 0) == 0
+    assert L.dsa_index_topk(fake, *args, 2049, good, good, good, 1 << 30, None) == 2
+    assert L.dsa_index_topk_workspace_size(fake, 4, 1, 2049, 0) == 0
 
 
 def test_context_creation_without_gpu_fails_cleanly(L):
