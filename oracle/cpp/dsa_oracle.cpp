@@ -33,9 +33,15 @@
 //          y'_i = y_i c - y_{i+64} s,  y'_{i+64} = y_{i+64} c + y_i s
 //   optional Hadamard: fp32 butterflies h = 1, 2, ..., 64, (a, b) -> (a+b, a-b)
 //   bf16 = round to nearest even; fp8: scale = max(max|y'|, 1e-4) / 448,
-//          code = e4m3(y' * (1/scale)) rounded to nearest even, saturating.
+//          code = e4m3(y' * (1/scale)) rounded to nearest even, saturating;
+//   fp4  = the same with 6 and e2m1 (OCP MX v1.0 FP4 element: bias 1, one
+//          mantissa bit, largest 6), two codes per byte, the even dimension
+//          in the low nibble (64 B + 4 B scale per token). The pages name an
+//          fp4 variant ("The Fused Kernel Decision", section "The Message: A
+//          Blueprint for Kernel Modification") without a layout: this is the
+//          fp8 key with e2m1 elements.
 // Scores: s = sum_h w_h * max(0, q_h . k) in double, k the stored key exactly
-// (bf16 value, or e4m3 value times its scale); with the Hadamard rotation the
+// (bf16 value, or e4m3 / e2m1 value times its scale); with the Hadamard rotation the
 // query heads are rotated exactly by the +-1 Sylvester matrix and the dot
 // products divided by 128. Each dot product is summed over d in order.
 // Top-k: the visible keys sorted by (score desc, position asc), the first
@@ -57,7 +63,9 @@ constexpr int H = 64;
 constexpr int PAGE = 64;
 constexpr int FMT_BF16 = 0;
 constexpr int FMT_FP8 = 1;
-constexpr long long kPageBytes[2] = {PAGE * D * 2, PAGE * D + PAGE * 4};
+constexpr int FMT_FP4 = 2;
+constexpr long long kPageBytes[3] = {PAGE * D * 2, PAGE * D + PAGE * 4, PAGE * D / 2 + PAGE * 4};
+constexpr long long kCodeBytes[3] = {0, D, D / 2};  // per token, before the page's scales
 
 float f32_of_bits(uint32_t b) {
   float f;
@@ -123,6 +131,35 @@ uint8_t e4m3_round(float xf) {
     code = static_cast<uint8_t>(((Ev + 7) << 3) | m);
   }
   return neg ? static_cast<uint8_t>(code | 0x80) : code;
+}
+
+// OCP E2M1 code (low 4 bits) -> value: bias 1, one mantissa bit, no NaN
+double e2m1_value(uint8_t c) {
+  const int e = (c >> 1) & 3, m = c & 1;
+  const double v = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return (c & 8) ? -v : v;
+}
+
+// binary32 -> E2M1 code, nearest with ties to even, saturating at +-6. The
+// representable magnitudes are the multiples of 0.5 up to 2, of 1 up to 4
+// and of 2 up to 6; a tie goes to the even multiple, which is the even code.
+uint8_t e2m1_round(float xf) {
+  const double x = xf;
+  const bool neg = std::signbit(x);
+  const double a = std::fabs(x);
+  const double q = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+  const double v = std::min(std::nearbyint(a / q) * q, 6.0);
+  uint8_t code;
+  if (v < 1.0)
+    code = static_cast<uint8_t>(v * 2.0);  // 0 or 0.5: subnormal codes 0, 1
+  else {
+    int ev = 0;
+    std::frexp(v, &ev);  // v = f * 2^ev, f in [0.5, 1)
+    const int E = ev - 1;
+    const int m = static_cast<int>(std::lrint((v / std::ldexp(1.0, E) - 1.0) * 2.0));
+    code = static_cast<uint8_t>(((E + 1) << 1) | m);
+  }
+  return neg ? static_cast<uint8_t>(code | 8) : code;
 }
 
 // Run f(i) for i in [0, n) on nthreads threads (dynamic, in chunks).
@@ -192,11 +229,16 @@ void store_token(uint8_t* cache, int fmt, const uint16_t* kr, int pos, long long
     float amax = 0.0f;
     for (int d = 0; d < D; ++d) amax = std::max(amax, std::fabs(o[d]));
     amax = std::max(amax, 1e-4f);
-    const float scale = amax / 448.0f;
+    const float scale = amax / (fmt == FMT_FP8 ? 448.0f : 6.0f);
     const float inv = 1.0f / scale;
-    uint8_t* dst = pg + static_cast<long long>(off) * D;
-    for (int d = 0; d < D; ++d) dst[d] = e4m3_round(o[d] * inv);
-    std::memcpy(pg + PAGE * D + off * 4, &scale, 4);
+    const long long cb = kCodeBytes[fmt];
+    uint8_t* dst = pg + static_cast<long long>(off) * cb;
+    if (fmt == FMT_FP8)
+      for (int d = 0; d < D; ++d) dst[d] = e4m3_round(o[d] * inv);
+    else
+      for (int d = 0; d < D; d += 2)
+        dst[d / 2] = static_cast<uint8_t>(e2m1_round(o[d] * inv) | (e2m1_round(o[d + 1] * inv) << 4));
+    std::memcpy(pg + PAGE * cb + off * 4, &scale, 4);
   }
 }
 
@@ -239,7 +281,7 @@ void read_key(const TopkArgs& a, int b, long long p, double* k) {
   if (a.fmt == FMT_BF16) {
     const uint16_t* src = reinterpret_cast<const uint16_t*>(pg + static_cast<long long>(off) * D * 2);
     for (int d = 0; d < D; ++d) k[d] = bf16_value(src[d]);
-  } else {
+  } else if (a.fmt == FMT_FP8) {
     static const std::vector<double> table = [] {  // every code's exact value
       std::vector<double> t(256);
       for (int c = 0; c < 256; ++c) t[c] = e4m3_value(static_cast<uint8_t>(c));
@@ -249,6 +291,14 @@ void read_key(const TopkArgs& a, int b, long long p, double* k) {
     std::memcpy(&scale, pg + PAGE * D + off * 4, 4);
     const uint8_t* src = pg + static_cast<long long>(off) * D;
     for (int d = 0; d < D; ++d) k[d] = table[src[d]] * static_cast<double>(scale);
+  } else {
+    float scale;
+    std::memcpy(&scale, pg + PAGE * (D / 2) + off * 4, 4);
+    const uint8_t* src = pg + static_cast<long long>(off) * (D / 2);
+    for (int d = 0; d < D; d += 2) {
+      k[d] = e2m1_value(src[d / 2] & 0xF) * static_cast<double>(scale);
+      k[d + 1] = e2m1_value(src[d / 2] >> 4) * static_cast<double>(scale);
+    }
   }
 }
 
@@ -358,7 +408,7 @@ int dso_hardware_threads() {
 int dso_store(uint8_t* cache, int num_pages, int fmt, const uint16_t* k_raw, const int32_t* pos,
               const int32_t* seq, long long T, const int32_t* page_table, int B, int max_pages,
               float theta, float eps, const uint16_t* gamma_bf16, int hadamard, int nthreads) {
-  if (fmt != FMT_BF16 && fmt != FMT_FP8) return -1;
+  if (fmt != FMT_BF16 && fmt != FMT_FP8 && fmt != FMT_FP4) return -1;
   std::vector<long long> page(static_cast<size_t>(T));
   for (long long t = 0; t < T; ++t) {
     if (seq[t] < 0 || seq[t] >= B || pos[t] < 0 || pos[t] >= static_cast<long long>(max_pages) * PAGE)
@@ -382,7 +432,7 @@ int dso_topk(const uint8_t* cache, int fmt, const int32_t* page_table, int B, in
              int causal, int k, int hadamard, const long long* rows, long long nrows,
              int32_t* out_idx, float* out_score, double* full, const long long* full_off,
              int nthreads) {
-  if ((fmt != FMT_BF16 && fmt != FMT_FP8) || k < 1) return -1;
+  if ((fmt != FMT_BF16 && fmt != FMT_FP8 && fmt != FMT_FP4) || k < 1) return -1;
   TopkArgs a{cache, fmt, page_table, max_pages, seq_lens, cu_q, B, q, w, causal, k, hadamard};
   parallel_for(nrows, nthreads, 1, [&](long long i) {
     const long long row = rows[i];

@@ -7,7 +7,7 @@ product, applies a ReLU, and keeps the top-K key positions, K = 512 or 1024):
 
   s[q, key] = sum_h  w[q, h] * max(0, sum_d q[q, h, d] * k[key, d])
 
-with k the stored key value (bf16, or the e4m3 code times the token's fp32
+with k the stored key value (bf16, or the e4m3 or e2m1 code times the token's fp32
 scale, decoded exactly). The head-weighted sum and the causal rule are the
 plainest reading the pages leave open: a query at position p sees keys
 0..p of its own sequence (all keys 0..L-1 when not causal). Queries of

@@ -11,6 +11,10 @@ maps to a page and an offset inside it):
   bf16 : store round(y') as 128 bf16 values                   (256 B/token)
   fp8  : scale = max|y'| / 448, store e4m3(y' / scale) (128 B) and the fp32
          scale (4 B)                                          (132 B/token)
+  fp4  : scale = max|y'| / 6, store e2m1(y' / scale) two codes per byte
+         (64 B) and the fp32 scale (4 B)                      (68 B/token)
+         (the pages name an fp4 variant but give no layout: this reading
+         is the fp8 key with e2m1 elements, see oracle.formats)
 
 The bytes are decided by floating point, so the oracle computes them in the
 precision the kernel uses (fp32) with one fixed order of operations, which is
@@ -29,6 +33,7 @@ the definition the stored bytes are compared against:
     every product and sum rounded separately (no fused multiply-add);
   * fp8: amax = max(max_d |y'_d|, 1e-4); scale = amax / 448;
     inv = 1 / scale; code_d = e4m3_satfinite(y'_d * inv).
+  * fp4: the same with 6 for 448 and e2m1_satfinite for e4m3_satfinite.
 
 The 1e-4 floor on amax is this library's reading for an all-zero key (the
 pages do not say); it keeps the scale positive, which the scorer relies on.
@@ -48,6 +53,7 @@ way gives (H q) . (H k) = 128 (q . k); the scorer divides by 128 (exact).
 Cache layouts (per page of 64 tokens):
   bf16 : [64][128] bf16                         16384 bytes
   fp8  : [64][128] e4m3, then [64] fp32 scales   8448 bytes
+  fp4  : [64][64] e2m1 pairs, then [64] fp32 scales  4352 bytes
 """
 from __future__ import annotations
 
@@ -62,8 +68,10 @@ HALF = 64
 PAGE = 64
 FMT_BF16 = 0
 FMT_FP8 = 1
-PAGE_BYTES = {FMT_BF16: PAGE * D * 2, FMT_FP8: PAGE * D + PAGE * 4}
-TOKEN_BYTES = {FMT_BF16: D * 2, FMT_FP8: D + 4}
+FMT_FP4 = 2
+PAGE_BYTES = {FMT_BF16: PAGE * D * 2, FMT_FP8: PAGE * D + PAGE * 4, FMT_FP4: PAGE * D // 2 + PAGE * 4}
+TOKEN_BYTES = {FMT_BF16: D * 2, FMT_FP8: D + 4, FMT_FP4: D // 2 + 4}
+CODE_BYTES = {FMT_FP8: D, FMT_FP4: D // 2}  # per token, before the page's scales
 AMAX_FLOOR = np.float32(1e-4)
 
 
@@ -156,6 +164,15 @@ def quantize_fp8(yr: np.ndarray):
     return codes, scale
 
 
+def quantize_fp4(yr: np.ndarray):
+    """Per-token amax scale and packed e2m1 codes [T,64] of fp32 rows."""
+    amax = np.maximum(np.max(np.abs(yr), axis=1), AMAX_FLOOR).astype(np.float32)
+    scale = (amax / np.float32(F.E2M1_MAX)).astype(np.float32)
+    inv = (np.float32(1.0) / scale).astype(np.float32)
+    codes = F.f32_to_e2m1_satfinite(yr * inv[:, None])
+    return F.pack_e2m1(codes), scale
+
+
 def new_cache(num_pages: int, fmt: int) -> np.ndarray:
     return np.zeros(num_pages * PAGE_BYTES[fmt], dtype=np.uint8)
 
@@ -172,13 +189,15 @@ def slots(pos: np.ndarray, seq: np.ndarray, page_table: np.ndarray, num_pages: i
 
 def _views(cache: np.ndarray, fmt: int):
     """Per-page views of the cache bytes: bf16 -> [pages, 64, 256] bytes;
-    fp8 -> ([pages, 64, 128] codes, [pages, 64] fp32 scales)."""
+    fp8 -> ([pages, 64, 128] codes, [pages, 64] fp32 scales); fp4 ->
+    ([pages, 64, 64] packed codes, [pages, 64] fp32 scales)."""
     pb = PAGE_BYTES[fmt]
     pages = cache.reshape(-1, pb)
     if fmt == FMT_BF16:
         return pages.reshape(-1, PAGE, 2 * D), None
-    data = pages[:, :PAGE * D].reshape(-1, PAGE, D)
-    scales = pages[:, PAGE * D:].view("<f4")
+    cb = CODE_BYTES[fmt]
+    data = pages[:, :PAGE * cb].reshape(-1, PAGE, cb)
+    scales = pages[:, PAGE * cb:].view("<f4")
     return data, scales
 
 
@@ -193,14 +212,15 @@ def store(cache: np.ndarray, fmt: int, k_raw_bits, pos, seq, page_table, num_pag
     if fmt == FMT_BF16:
         data[page, off] = F.f32_to_bf16(yr).view(np.uint8).reshape(-1, 2 * D)
     else:
-        codes, scale = quantize_fp8(yr)
+        codes, scale = quantize_fp8(yr) if fmt == FMT_FP8 else quantize_fp4(yr)
         data[page, off] = codes
         scales[page, off] = scale
 
 
 def read_keys(cache: np.ndarray, fmt: int, page_table_row: np.ndarray, n: int) -> np.ndarray:
     """Exact float64 values of the stored keys at positions 0..n-1 of one
-    sequence (fp8: e4m3 value times the token's scale, exact in double)."""
+    sequence (fp8 / fp4: the e4m3 / e2m1 value times the token's scale,
+    exact in double)."""
     if n == 0:
         return np.zeros((0, D))
     pos = np.arange(n, dtype=np.int64)
@@ -209,4 +229,6 @@ def read_keys(cache: np.ndarray, fmt: int, page_table_row: np.ndarray, n: int) -
     data, scales = _views(cache, fmt)
     if fmt == FMT_BF16:
         return F.bf16_to_f64(np.ascontiguousarray(data[page, off]).view(np.uint16))
-    return F.e4m3_to_f64(data[page, off]) * scales[page, off].astype(np.float64)[:, None]
+    codes = data[page, off]
+    vals = F.e4m3_to_f64(codes) if fmt == FMT_FP8 else F.e2m1_to_f64(F.unpack_e2m1(codes))
+    return vals * scales[page, off].astype(np.float64)[:, None]

@@ -1,6 +1,7 @@
-"""Pins for the oracle's number formats (bf16, OCP E4M3), against the formats'
-definitions, a hand-written table from the OCP FP8 specification, and
-torch's own CPU conversions as an independent library routine."""
+"""Pins for the oracle's number formats (bf16, OCP E4M3, OCP MX E2M1),
+against the formats' definitions, hand-written tables from the OCP FP8 and
+MX specifications, and torch's own CPU conversions as an independent library
+routine."""
 import os
 
 import numpy as np
@@ -107,3 +108,65 @@ def test_bf16_decode_exact():
     v = F.bf16_to_f64(bits)
     fin = np.isfinite(v)
     assert np.array_equal(F.f32_to_bf16(v[fin].astype(np.float32)), bits[fin])
+
+
+def _golden_e2m1():
+    rows = []
+    with open(os.path.join(GOLD, "e2m1_codes.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            v, c = line.split()[:2]
+            rows.append((float(v), int(c, 16)))
+    return rows
+
+
+def test_e2m1_golden_table():
+    rows = _golden_e2m1()
+    vals = np.array([v for v, _ in rows], dtype=np.float32)
+    want = [c for _, c in rows]
+    assert F.f32_to_e2m1_satfinite(vals).tolist() == want
+
+
+def test_e2m1_decode_by_formula():
+    # value = (-1)^s 2^(e-1) (1 + m/2), subnormal m/2, enumerated by hand loops
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = F.e2m1_to_f64(np.arange(16, dtype=np.uint8))
+    assert got[:8].tolist() == want
+    assert got[8:].tolist() == [-v for v in want]
+    for c in range(16):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        v = m / 2.0 if e == 0 else 2.0 ** (e - 1) * (1 + m / 2.0)
+        assert got[c] == (-v if s else v)
+
+
+def test_e2m1_all_codes_roundtrip():
+    codes = np.arange(16, dtype=np.uint8)
+    v = F.e2m1_to_f64(codes)
+    assert np.array_equal(F.f32_to_e2m1_satfinite(v.astype(np.float32)), codes)
+
+
+def test_e2m1_nearest_bruteforce():
+    # the code whose value is nearest |x| (ties: even code), by exhaustive search
+    table = F.e2m1_to_f64(np.arange(8, dtype=np.uint8))
+    rng = np.random.default_rng(4)
+    x = np.abs(rng.standard_normal(4000) * np.exp(rng.uniform(-3, 3, 4000))).astype(np.float32)
+    x = np.concatenate([x, (np.arange(0, 29) / 4.0).astype(np.float32)])  # every quarter to 7
+    got = F.f32_to_e2m1_satfinite(x)
+    for xi, gi in zip(x.astype(np.float64), got):
+        if xi >= 6:
+            assert gi == 0x7
+            continue
+        d = np.abs(table - xi)
+        best = np.nonzero(d == d.min())[0]
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert gi == want
+
+
+def test_e2m1_pack_nibble_order():
+    # element 2i sits in the low nibble of byte i
+    codes = np.array([[0x1, 0x7, 0x8, 0xF, 0x2, 0x0]], np.uint8)
+    p = F.pack_e2m1(codes)
+    assert p.tolist() == [[0x71, 0xF8, 0x02]]
+    assert np.array_equal(F.unpack_e2m1(p), codes)

@@ -27,12 +27,23 @@ def _decode_key_by_hand(cache, fmt, page, off):
         base = page * 16384 + off * 256
         bits = cache[base:base + 256].view(np.uint16)
         return [float(v) for v in F.bf16_to_f64(bits)]
-    base = page * 8448 + off * 128
-    sc = float(cache[page * 8448 + 8192 + off * 4: page * 8448 + 8196 + off * 4].view("<f4")[0])
-    return [float(v) * sc for v in F.e4m3_to_f64(cache[base:base + 128])]
+    if fmt == S.FMT_FP8:
+        base = page * 8448 + off * 128
+        sc = float(cache[page * 8448 + 8192 + off * 4: page * 8448 + 8196 + off * 4].view("<f4")[0])
+        return [float(v) * sc for v in F.e4m3_to_f64(cache[base:base + 128])]
+    # fp4: 64 bytes of code pairs (even dimension in the low nibble), then the
+    # page's 64 scales; the E2M1 magnitudes written out by hand
+    mag = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    base = page * 4352 + off * 64
+    sc = float(cache[page * 4352 + 4096 + off * 4: page * 4352 + 4100 + off * 4].view("<f4")[0])
+    out = []
+    for byte in cache[base:base + 64].tolist():
+        for c in (byte & 0xF, byte >> 4):
+            out.append((-1.0 if c & 8 else 1.0) * mag[c & 7] * sc)
+    return out
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 @pytest.mark.parametrize("causal", [True, False])
 def test_bruteforce_tiny(fmt, causal):
     wl = I.make_workload("bf", [70, 40], [3, 2], [70, 40], causal, 16, seed=3, wid=11)
@@ -91,7 +102,7 @@ def test_select_topk_full_sort_with_ties():
         assert np.array_equal(val[:len(want)], s[want])
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_invariants(fmt):
     wl = I.make_workload("inv", [700, 333], [40, 9], [700, 333], True, 64, seed=5, wid=12)
     cache = _store(wl, fmt)

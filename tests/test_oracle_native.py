@@ -22,7 +22,7 @@ def _both_caches(wl, fmt, hadamard=False, gamma=None):
 
 
 @pytest.mark.parametrize("hadamard", [False, True])
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_store_bytes_equal_numpy_oracle(fmt, hadamard):
     rng = np.random.default_rng(11)
     T = 1500
@@ -47,7 +47,7 @@ def test_store_bytes_equal_numpy_oracle_long_positions():
     wl.fill_pos = wl.fill_pos[:0]
     wl.fill_seq = wl.fill_seq[:0]
     wl.fill_k = wl.fill_k[:0]
-    for fmt in (S.FMT_BF16, S.FMT_FP8):
+    for fmt in (S.FMT_BF16, S.FMT_FP8, S.FMT_FP4):
         a, b = _both_caches(wl, fmt)
         assert np.array_equal(a, b)
 
@@ -78,20 +78,20 @@ def _compare_topk(wl, fmt, hadamard=False, k=None):
         assert np.all(np.abs(nfull[r] - s) <= 1e-12 * m)
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_topk_equals_numpy_oracle_prefill(fmt):
     wl = I.make_workload("ntp", [300, 777, 129], [300, 40, 129], [300, 777, 129], True, 128,
                          seed=13, wid=13)
     _compare_topk(wl, fmt)
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_topk_equals_numpy_oracle_decode_non_causal(fmt):
     wl = I.make_workload("ntd", [2000, 700, 64], [1, 3, 2], [1, 3, 2], False, 512, seed=14, wid=14)
     _compare_topk(wl, fmt)
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_topk_equals_numpy_oracle_hadamard(fmt):
     wl = I.make_workload("nth", [600, 200], [5, 3], [600, 200], True, 64, seed=15, wid=15)
     _compare_topk(wl, fmt, hadamard=True)
@@ -110,7 +110,7 @@ def test_topk_ties_broken_by_position():
 def test_bruteforce_tiny():
     # pure-Python scores and a full sort, on 70 keys and 3 queries (signed w)
     wl = I.make_workload("ntb", [70], [3], [70], True, 16, seed=17, wid=17)
-    for fmt in (S.FMT_BF16, S.FMT_FP8):
+    for fmt in (S.FMT_BF16, S.FMT_FP8, S.FMT_FP4):
         cache = N.new_cache(wl.num_pages, fmt)
         N.store(cache, fmt, wl.new_k, wl.new_pos, wl.new_seq, wl.page_table, wl.num_pages)
         ni, ns, full = N.index_topk(cache, fmt, wl.page_table, wl.seq_lens, wl.cu_q, wl.q, wl.head_w,

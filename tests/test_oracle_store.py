@@ -197,7 +197,59 @@ def test_fp8_zero_token():
     assert scale[0] == np.float32(np.float32(1e-4) / np.float32(448))
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+def test_fp4_roundtrip_bound_and_amax_code():
+    rng = np.random.default_rng(6)
+    T = 3000
+    kb = _bf16(rng.standard_normal((T, 128)) * np.exp(rng.uniform(-5, 5, (T, 128))))
+    yr = S.normalize_rotate(kb, rng.integers(0, 5000, T), 10000.0, 1e-6)
+    packed, scale = S.quantize_fp4(yr)
+    assert packed.shape == (T, 64)
+    deq = F.e2m1_to_f64(F.unpack_e2m1(packed)) * scale[:, None].astype(np.float64)
+    y = yr.astype(np.float64)
+    # e2m1 keeps 2 significant bits: relative error <= 1/4 above 1 (scaled),
+    # absolute error <= 1/4 of the scale below it
+    bound = np.maximum(0.25 * np.abs(y), 0.25 * scale[:, None])
+    assert np.all(np.abs(y - deq) <= bound * (1 + 1e-6))
+    # the largest element of each token maps to +-6
+    am = np.argmax(np.abs(y), axis=1)
+    top = F.unpack_e2m1(packed)[np.arange(T), am]
+    assert np.all((top & 0x7) == 0x7)
+    assert np.allclose(scale, np.abs(y).max(axis=1) / 6, rtol=2 * ULP32)
+
+
+def test_fp4_zero_token():
+    yr = np.zeros((1, 128), np.float32)
+    packed, scale = S.quantize_fp4(yr)
+    assert np.all(packed == 0)
+    assert scale[0] == np.float32(np.float32(1e-4) / np.float32(6))
+
+
+def test_fp4_one_hot_hand_example():
+    # raw key a * e_j at position 0 (RoPE is the identity there): RMSNorm gives
+    # y_j = a / sqrt(a^2/128 + eps), every other dim 0; amax = |y_j|, so
+    # element j is +-6 (code 0x7 / 0xF), every other code 0, and the scale is
+    # |y_j| / 6. With j = 5 the code sits in the high nibble of byte 2.
+    a, j = -2.0, 5
+    x = np.zeros((1, 128), np.float32)
+    x[0, j] = a
+    yr = S.normalize_rotate(_bf16(x), np.array([0]), 10000.0, 1e-6)
+    yj = np.float32(a) * (np.float32(1) / np.sqrt(np.float32(a * a) * np.float32(1 / 128) + np.float32(1e-6)))
+    assert yr[0, j] == yj
+    packed, scale = S.quantize_fp4(yr)
+    want = np.zeros(64, np.uint8)
+    want[2] = 0xF << 4
+    assert np.array_equal(packed[0], want)
+    assert scale[0] == np.float32(np.abs(yj) / np.float32(6))
+    # and the same bytes through the paged store: page 3, slot 0
+    cache = S.new_cache(4, S.FMT_FP4)
+    S.store(cache, S.FMT_FP4, _bf16(x), np.array([0]), np.array([0]), np.array([[3]], np.int32), 4)
+    base = 3 * 4352
+    assert np.array_equal(cache[base:base + 64], want)
+    assert cache[base + 4096:base + 4100].view("<f4")[0] == scale[0]
+    assert not cache[:base].any() and not cache[base + 64:base + 4096].any()
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_paged_store_placement_and_permutation(fmt):
     wl = I.make_workload("t", [300, 130], [1, 1], [300, 130], True, 512, seed=7, wid=9)
     cache = S.new_cache(wl.num_pages, fmt)
@@ -223,15 +275,21 @@ def test_paged_store_placement_and_permutation(fmt):
     if fmt == S.FMT_BF16:
         off = page * 16384 + (p % 64) * 256
         assert np.array_equal(cache[off:off + 256].view(np.uint16), F.f32_to_bf16(yr)[0])
-    else:
+    elif fmt == S.FMT_FP8:
         codes, sc = S.quantize_fp8(yr)
         off = page * 8448 + (p % 64) * 128
         assert np.array_equal(cache[off:off + 128], codes[0])
         so = page * 8448 + 8192 + (p % 64) * 4
         assert cache[so:so + 4].view("<f4")[0] == sc[0]
+    else:
+        codes, sc = S.quantize_fp4(yr)
+        off = page * 4352 + (p % 64) * 64
+        assert np.array_equal(cache[off:off + 64], codes[0])
+        so = page * 4352 + 4096 + (p % 64) * 4
+        assert cache[so:so + 4].view("<f4")[0] == sc[0]
     # the last page of sequence 1 (130 tokens -> 3 pages, 2 slots used) keeps zeros
     last = int(wl.page_table[1, 2])
-    tb = S.TOKEN_BYTES[fmt] if fmt == S.FMT_BF16 else 128
+    tb = S.TOKEN_BYTES[fmt] if fmt == S.FMT_BF16 else S.CODE_BYTES[fmt]
     base = last * S.PAGE_BYTES[fmt]
     assert np.all(cache[base + 2 * tb: base + 64 * tb] == 0)
 
