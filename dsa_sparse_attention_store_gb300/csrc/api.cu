@@ -49,6 +49,7 @@ const char* dsa_status_str(dsa_status s) {
 size_t dsa_cache_page_bytes(dsa_fmt fmt) {
   if (fmt == DSA_FMT_BF16) return DSA_PAGE_SIZE * DSA_HEAD_DIM * 2;
   if (fmt == DSA_FMT_FP8) return DSA_PAGE_SIZE * DSA_HEAD_DIM + DSA_PAGE_SIZE * 4;
+  if (fmt == DSA_FMT_FP4) return DSA_PAGE_SIZE * DSA_HEAD_DIM / 2 + DSA_PAGE_SIZE * 4;
   return 0;
 }
 
@@ -210,7 +211,7 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
                            int32_t B, int32_t max_pages, void* cache, int32_t num_pages,
                            dsa_fmt fmt, dsa_stream_t stream) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
-  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return DSA_ERR_UNSUPPORTED;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8 && fmt != DSA_FMT_FP4) return DSA_ERR_UNSUPPORTED;
   if (T < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
   if (T == 0) return DSA_OK;
   if (!k_raw || !rope_pos || !seq_id || !page_table || !cache) return DSA_ERR_INVALID_ARG;
@@ -225,7 +226,7 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
 size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k,
                                      dsa_fmt fmt) {
   if (!ctx || Tq < 0 || B <= 0 || k < 1 || k > 2048) return 0;
-  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return 0;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8 && fmt != DSA_FMT_FP4) return 0;
   return dsa::topk_workspace(ctx, Tq, B, k, fmt);
 }
 
@@ -236,7 +237,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
                           float* out_score, void* workspace, size_t ws_bytes,
                           dsa_stream_t stream) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
-  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return DSA_ERR_UNSUPPORTED;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8 && fmt != DSA_FMT_FP4) return DSA_ERR_UNSUPPORTED;
   if (k < 1 || k > 2048) return DSA_ERR_UNSUPPORTED;
   if (Tq < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(num_pages) * 64 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;

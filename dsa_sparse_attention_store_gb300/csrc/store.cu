@@ -1,5 +1,5 @@
-// Index-key store kernel: RMSNorm + RoPE + (e4m3 with a per-token scale |
-// bf16) written into a 64-token paged cache.
+// Index-key store kernel: RMSNorm + RoPE + (e4m3 or e2m1 with a per-token
+// scale | bf16) written into a 64-token paged cache.
 //
 // What it computes follows "The Moment of Validation: Diagnosing an OOM Crash
 // in the bf16 Index-K Fix for DeepSeek V4 Sparse Attention" (section "Input
@@ -9,8 +9,8 @@
 // to a page and an offset, a bf16 page is [64*128]).
 //
 // Mapping: one token per half-warp. Lane l (0..15) owns dims 8l..8l+7 and
-// moves them with one 16-byte load and one 16-byte (bf16) or 8-byte (fp8)
-// store, so a warp reads 512 contiguous bytes per instruction. The sum of
+// moves them with one 16-byte load and one 16-byte (bf16), 8-byte (fp8) or
+// 4-byte (fp4) store, so a warp reads 512 contiguous bytes per instruction. The sum of
 // squares is 8 sequential fused multiply-adds per lane (exact products of
 // bf16 inputs) followed by a xor butterfly over the half-warp (8, 4, 2, 1):
 // this order is the store's definition, which is what makes the bytes
@@ -24,6 +24,7 @@
 // dims and h = 8, 16, 32, 64 between lanes l and l ^ (h/8), each pair
 // (i, i+h) becoming (a + b, a - b) in fp32.
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "internal.cuh"
@@ -163,9 +164,25 @@ __global__ void __launch_bounds__(256) store_kernel(
 #pragma unroll
     for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
     amax = fmaxf(amax, 1e-4f);
-    const float scale = __fdiv_rn(amax, 448.0f);
+    constexpr bool E4M3 = FMT == DSA_FMT_FP8;
+    const float scale = __fdiv_rn(amax, E4M3 ? 448.0f : 6.0f);
     const float inv = __fdiv_rn(1.0f, scale);
-    if (ok) {
+    if (!E4M3 && ok) {
+      // fp4: 8 e2m1 codes in one word, dimension 8l + 2v in the low nibble
+      // of byte v (round to nearest even, saturating at 6)
+      uint32_t w = 0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const __nv_fp4x2_storage_t p = __nv_cvt_float2_to_fp4x2(
+            make_float2(__fmul_rn(o[2 * v], inv), __fmul_rn(o[2 * v + 1], inv)), __NV_E2M1,
+            cudaRoundNearest);
+        w |= static_cast<uint32_t>(p) << (8 * v);
+      }
+      uint8_t* pg = cache + static_cast<long long>(page) * (kPage * kD / 2 + kPage * 4);
+      __stcs(reinterpret_cast<unsigned int*>(pg + off * (kD / 2) + 4 * l), w);
+      if (l == 0) __stcs(reinterpret_cast<float*>(pg + kPage * kD / 2 + off * 4), scale);
+    }
+    if (E4M3 && ok) {
       uint32_t w[2];
 #pragma unroll
       for (int v = 0; v < 2; ++v) {
@@ -194,7 +211,8 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
   const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
   LaunchScope scope(ctx, DSA_K_STORE, stream);
   auto kern = fmt == DSA_FMT_BF16 ? (ctx->hadamard ? store_kernel<DSA_FMT_BF16, true> : store_kernel<DSA_FMT_BF16, false>)
-                                  : (ctx->hadamard ? store_kernel<DSA_FMT_FP8, true> : store_kernel<DSA_FMT_FP8, false>);
+               : fmt == DSA_FMT_FP8 ? (ctx->hadamard ? store_kernel<DSA_FMT_FP8, true> : store_kernel<DSA_FMT_FP8, false>)
+                                    : (ctx->hadamard ? store_kernel<DSA_FMT_FP4, true> : store_kernel<DSA_FMT_FP4, false>);
   const cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, stream,
                                    static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B,
                                    max_pages, static_cast<uint8_t*>(cache), num_pages,

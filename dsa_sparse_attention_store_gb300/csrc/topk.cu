@@ -63,6 +63,7 @@ constexpr int kH = 64;
 constexpr int kD = 128;
 constexpr int kTile = 128;  // keys per MMA tile = 2 pages
 constexpr int kPageBytesFp8 = 64 * 128 + 64 * 4;
+constexpr int kPageBytesFp4 = 64 * 64 + 64 * 4;
 
 // The work is split evenly in units: a query tile with n key tiles costs
 // n + ovh units, ovh standing for its fixed costs (query load, final merge
@@ -432,6 +433,22 @@ __device__ __forceinline__ void prep_row(uint8_t* sQ, int r, float* sw, int lane
   }
 }
 
+// ------------------------------------------------------------------ fp4 keys
+// Eight e2m1 codes (a 32-bit word, code i in bits 4i .. 4i+3: sign, two
+// exponent bits with bias 1, one mantissa bit) to eight e4m3 bytes, code i
+// in byte i of lo (i < 4) or hi. Every e2m1 value is an e4m3 value, so this
+// is a table: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are the e4m3 codes
+// 0x00, 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C (bias 7: 0.5 = 2^-1 is
+// exponent field 6), looked up by byte permutation on the low three bits of
+// each code; the sign moves from bit 3 of the code to bit 7 of the byte.
+__device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  constexpr uint32_t kMag0 = 0x3C383000u, kMag1 = 0x4C484440u;
+  // a selector nibble's fourth bit is ignored: each picks byte (nibble & 7)
+  const uint32_t s = (w >> 3) & 0x11111111u;  // code i's sign at bit 4i
+  lo = __byte_perm(kMag0, kMag1, w) | __byte_perm(0x8000u, 0u, s);
+  hi = __byte_perm(kMag0, kMag1, w >> 16) | __byte_perm(0x8000u, 0u, s >> 16);
+}
+
 // ------------------------------------------------------------------ scorer configuration
 template <int QT, int FMT, int KSEL, int NQ>
 struct Cfg {
@@ -449,8 +466,17 @@ struct Cfg {
   // per SM to cover the HBM latency of a streaming one-query tile
   // (four-query tiles selecting 1024 keys trade a stage for a candidate
   // buffer twice the selection: a smaller buffer would select every tile)
-  static constexpr int S = QT == 4 ? (FMT == DSA_FMT_BF16 ? (KSEL > 512 ? 2 : 3) : (KSEL > 512 ? 4 : 6))
-                                   : (FMT == DSA_FMT_BF16 ? 4 : 6);
+  // fp4 keys: the tile's e2m1 codes land in a ring of their own (NR slots
+  // of 8 KB, the bytes in flight) and the converter warps widen them into
+  // an operand stage, which then only has to cover the conversion and MMA
+  static constexpr bool FP4 = FMT == DSA_FMT_FP4;
+  static constexpr bool E8 = FMT != DSA_FMT_BF16;        // e4m3 operands (fp8, or widened fp4)
+  static constexpr int S = FP4 ? (QT == 4 ? 2 : 3)
+                               : QT == 4 ? (FMT == DSA_FMT_BF16 ? (KSEL > 512 ? 2 : 3) : (KSEL > 512 ? 4 : 6))
+                                         : (FMT == DSA_FMT_BF16 ? 4 : 6);
+  static constexpr int NR = FP4 ? (QT == 4 ? 3 : 6) : 0;  // raw fp4 tile slots
+  static constexpr int RAW_BYTES = kTile * 64;
+  static constexpr int NCV = FP4 ? 2 : 0;                 // converter warps
   static constexpr int NST = QT == 4 ? 6 : 16;           // score staging slots (tiles)
   // alternating groups each read their own ring of staging slots: a group
   // that skips the other's query tile must not wait on a slot phase that
@@ -466,7 +492,8 @@ struct Cfg {
   static_assert(TK >= KSEL + 2 * 128 + 128, "candidate buffer too small for the selection");
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
-  static constexpr int NWARPS = W_TOPK + 4 * NTK;
+  static constexpr int W_CONV = W_TOPK + 4 * NTK;          // first converter warp
+  static constexpr int NWARPS = W_CONV + NCV;
   static constexpr int NTHREADS = 32 * NWARPS;
   // TMEM accumulator buffers: the MMA of a tile waits for the score warps
   // to have read the buffer it reuses, so a deeper ring hides that round
@@ -474,11 +501,15 @@ struct Cfg {
   static constexpr int NTB = QT == 1 ? 4 : 2;
   static constexpr int TMEM_COLS = NTB * N;
   static constexpr int TERM_BYTES = N * 128 * (FMT == DSA_FMT_BF16 ? 2 : 1);  // one query term
+  // a page: its key codes, then its 64 fp32 scales (e4m3 / e2m1 keys)
+  static constexpr int PAGE_BYTES = FMT == DSA_FMT_FP8 ? kPageBytesFp8 : kPageBytesFp4;
+  static constexpr int SC_OFF = FMT == DSA_FMT_FP8 ? 64 * 128 : 64 * 64;
+  static_assert(PAGE_BYTES % 16 == 0 && SC_OFF % 16 == 0, "bulk copies start on 16-byte boundaries");
   static constexpr int Q_BYTES = NQ * TERM_BYTES;
   // the query tile arrives as the caller's bf16 rows (N x 256 bytes) and,
   // unless it is used as it is (bf16 cache, no rotation), the score warps
   // turn it into its terms in place
-  static constexpr bool PREP = FMT == DSA_FMT_FP8 || NQ > 1;
+  static constexpr bool PREP = E8 || NQ > 1;
   static constexpr bool HAD = FMT == DSA_FMT_BF16 ? NQ == 2 : NQ == 3;
   static_assert(!HAD || PREP, "the rotation is applied by the conversion");
   static constexpr int OP_BYTES = kTile * (FMT == DSA_FMT_BF16 ? 256 : 128);
@@ -493,10 +524,11 @@ struct Cfg {
   // pages come into a ring of their own by bulk copy beside the codes (the
   // score warps read them after the MMA has released the operand stage);
   // four-query tiles are slow enough per tile to load them from global memory
-  static constexpr bool SCALE_RING = FMT == DSA_FMT_FP8 && QT == 1;
+  static constexpr bool SCALE_RING = E8 && QT == 1;
   static constexpr int NSC = SCALE_RING ? 16 : 0;          // scale slots (tiles)
   static constexpr int OFF_SC = OFF_HIST + NTK * 512 * 4;  // after the radix-select histograms
-  static constexpr int OFF_MISC = OFF_SC + NSC * kTile * 4;
+  static constexpr int OFF_RAW = OFF_SC + NSC * kTile * 4;
+  static constexpr int OFF_MISC = OFF_RAW + NR * RAW_BYTES;
   static constexpr int MISC_BYTES = 2048;
   static constexpr int SMEM = OFF_MISC + MISC_BYTES + 1024;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -509,6 +541,7 @@ struct Misc {
   uint64_t tm_full[4], tm_empty[4], q_full, q_empty, fin, w_full[2], w_empty[2];
   uint64_t st_full[16], st_empty[16];
   uint64_t sc_full[16], sc_empty[16];
+  uint64_t raw_full[8], raw_empty[8];  // fp4 code slots
   uint64_t prep[2];  // the query tile of a weight buffer has been turned into its terms
   uint32_t tmem_base;
   int abort;
@@ -1040,6 +1073,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
   float* sSt = reinterpret_cast<float*>(sm + C::OFF_ST);
   float* sSc = reinterpret_cast<float*>(sm + C::OFF_SC);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(sm + C::OFF_HIST);
+  uint8_t* sRaw = sm + C::OFF_RAW;
   Misc* ms = reinterpret_cast<Misc*>(sm + C::OFF_MISC);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1047,8 +1081,14 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
-      mbar_init(&ms->op_full[i], 1);
+      // filled by the TMA (one arrival with the bytes) or, for fp4 keys, by
+      // every converter thread
+      mbar_init(&ms->op_full[i], C::FP4 ? 32 * C::NCV : 1);
       mbar_init(&ms->op_empty[i], 1);
+    }
+    for (int i = 0; i < C::NR; ++i) {
+      mbar_init(&ms->raw_full[i], 1);
+      mbar_init(&ms->raw_empty[i], 32 * C::NCV);
     }
     for (int i = 0; i < C::NTB; ++i) {
       mbar_init(&ms->tm_full[i], 1);
@@ -1164,12 +1204,20 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           const bool v1 = p1 >= 0 && p1 < a.num_pages;
           if ((2 * t < npg && !v0) || (2 * t + 1 < npg && !v1)) atomicOr(a.status, DSA_DEV_BOUNDS);
           const int slot = tile_seq % C::S, u = tile_seq / C::S;
-          if (!mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1)) {
+          const int rs = C::FP4 ? tile_seq % C::NR : 0, ur = C::FP4 ? tile_seq / C::NR : 0;
+          if (!(C::FP4 ? mbar_wait(&ms->raw_empty[rs], (ur & 1) ^ 1) : mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1))) {
             atomicOr(a.status, DSA_DEV_TIMEOUT);
             *abort_flag = 1;
           } else {
             uint8_t* dst = sOp + slot * C::OP_BYTES;
-            if constexpr (FMT == DSA_FMT_BF16) {
+            if constexpr (C::FP4) {
+              // a page's 64 x 64 code bytes are contiguous: one bulk copy each
+              // into the raw slot, widened by the converter warps
+              uint8_t* rdst = sRaw + rs * C::RAW_BYTES;
+              mbar_arrive_expect_tx(&ms->raw_full[rs], (v0 + v1) * 4096);
+              if (v0) bulk_load(rdst, a.cache + static_cast<long long>(p0) * C::PAGE_BYTES, 4096, &ms->raw_full[rs]);
+              if (v1) bulk_load(rdst + 4096, a.cache + static_cast<long long>(p1) * C::PAGE_BYTES, 4096, &ms->raw_full[rs]);
+            } else if constexpr (FMT == DSA_FMT_BF16) {
               // a page = two 64-column halves of 64 keys (128 B rows each)
               mbar_arrive_expect_tx(&ms->op_full[slot], (v0 + v1) * 16384);
               if (v0) {
@@ -1196,9 +1244,9 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
             }
             if (!*abort_flag) {
               mbar_arrive_expect_tx(&ms->sc_full[ss], (v0 + v1) * 256);
-              const uint8_t* sb = a.cache + 64 * 128;
-              if (v0) bulk_load(sSc + ss * kTile, sb + static_cast<long long>(p0) * kPageBytesFp8, 256, &ms->sc_full[ss]);
-              if (v1) bulk_load(sSc + ss * kTile + 64, sb + static_cast<long long>(p1) * kPageBytesFp8, 256, &ms->sc_full[ss]);
+              const uint8_t* sb = a.cache + C::SC_OFF;
+              if (v0) bulk_load(sSc + ss * kTile, sb + static_cast<long long>(p0) * C::PAGE_BYTES, 256, &ms->sc_full[ss]);
+              if (v1) bulk_load(sSc + ss * kTile + 64, sb + static_cast<long long>(p1) * C::PAGE_BYTES, 256, &ms->sc_full[ss]);
             }
           }
         }
@@ -1208,9 +1256,16 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     }
     // on abort, let this CTA's copies in flight land before the CTA exits
     if (lane == 0 && *abort_flag) {
-      for (int i = 1; i <= C::S && tile_seq - i >= 0; ++i) {
-        const int ts = tile_seq - i;
-        mbar_wait(&ms->op_full[ts % C::S], (ts / C::S) & 1, 20000000LL);
+      if constexpr (C::FP4) {
+        for (int i = 1; i <= C::NR && tile_seq - i >= 0; ++i) {
+          const int ts = tile_seq - i;
+          mbar_wait(&ms->raw_full[ts % C::NR], (ts / C::NR) & 1, 20000000LL);
+        }
+      } else {
+        for (int i = 1; i <= C::S && tile_seq - i >= 0; ++i) {
+          const int ts = tile_seq - i;
+          mbar_wait(&ms->op_full[ts % C::S], (ts / C::S) & 1, 20000000LL);
+        }
       }
       if constexpr (C::SCALE_RING) {
         for (int i = 1; i <= C::NSC && tile_seq - i >= 0; ++i) {
@@ -1309,7 +1364,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
         // queries
         float* sWp = sW + (seg_i & 1) * (QT * 64);
         for (int r = warp - C::W_SCORE; r < C::N; r += C::NSW)
-          prep_row<FMT == DSA_FMT_FP8, C::HAD, C::N, NQ>(sQ, r, sWp, lane);
+          prep_row<C::E8, C::HAD, C::N, NQ>(sQ, r, sWp, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ms->prep[seg_i & 1]);
@@ -1335,10 +1390,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
         return (v < 0 || v >= a.num_pages) ? -1 : v;
       };
       auto scale_of = [&](int id, int tt) -> float {
-        if constexpr (FMT == DSA_FMT_FP8 && !C::SCALE_RING) {
+        if constexpr (C::E8 && !C::SCALE_RING) {
           if (id >= 0)
-            return __ldg(reinterpret_cast<const float*>(a.cache + static_cast<long long>(id) * kPageBytesFp8 +
-                                                        64 * 128 + ((tt * kTile + row) & 63) * 4));
+            return __ldg(reinterpret_cast<const float*>(a.cache + static_cast<long long>(id) * C::PAGE_BYTES +
+                                                        C::SC_OFF + ((tt * kTile + row) & 63) * 4));
         }
         return 1.f;
       };
@@ -1410,7 +1465,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) unpack2(a2[i], acc[2 * i], acc[2 * i + 1]);
           float sc = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-          if constexpr (FMT == DSA_FMT_FP8) sc *= C::SCALE_RING ? rscale : kscale;
+          if constexpr (C::E8) sc *= C::SCALE_RING ? rscale : kscale;
           const int lim = j < s.nrows ? (a.causal ? s.qpos0 + j + 1 : s.L) : 0;
           if (pid < 0 || pos >= lim) sc = -__int_as_float(0x7f800000);
           scs[jj] = sc;
@@ -1437,6 +1492,55 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
       if (lane == 0) mbar_arrive(&ms->w_empty[seg_i & 1]);  // this warp is done with the weights
       ++seg_i;
     }
+  } else if (warp >= C::W_CONV) {
+    // ---------------------------------------------------------- fp4 converters
+    // Each thread widens 16-byte chunks of the tile (16 dims of one key row)
+    // from the raw slot's e2m1 pairs into the operand stage's e4m3 bytes,
+    // in the 128-byte swizzle the MMA reads (chunk c of row r at chunk
+    // c ^ (r & 7)); consecutive threads take consecutive chunks, so a warp
+    // reads and writes whole rows without bank conflicts.
+    if constexpr (C::FP4) {
+      const int ct = threadIdx.x - 32 * C::W_CONV;
+      int tile_seq = 0;
+      Seg s;
+      bool stop = false;
+      while (!stop && it.next(s)) {
+        for (int t = s.t0; t < s.t1; ++t) {
+          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+            stop = true;
+            break;
+          }
+          const int rs = tile_seq % C::NR, ur = tile_seq / C::NR;
+          const int slot = tile_seq % C::S, u = tile_seq / C::S;
+          if (!__all_sync(0xffffffffu, mbar_wait(&ms->raw_full[rs], ur & 1) &&
+                                           mbar_wait(&ms->op_empty[slot], (u & 1) ^ 1))) {
+            if (lane == 0) {
+              atomicOr(a.status, DSA_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+            stop = true;
+            break;
+          }
+          const uint2* src = reinterpret_cast<const uint2*>(sRaw + rs * C::RAW_BYTES);
+          uint8_t* dst = sOp + slot * C::OP_BYTES;
+#pragma unroll 4
+          for (int i = ct; i < kTile * 8; i += 32 * C::NCV) {
+            const int r = i >> 3, c = i & 7;
+            const uint2 w = src[i];  // row r, dims 16c .. 16c+15
+            uint4 o;
+            e2m1x8_to_e4m3(w.x, o.x, o.y);
+            e2m1x8_to_e4m3(w.y, o.z, o.w);
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+          }
+          // the stage is read by the tensor cores (async proxy)
+          fence_proxy_async_smem();
+          mbar_arrive(&ms->op_full[slot]);
+          mbar_arrive(&ms->raw_empty[rs]);
+          ++tile_seq;
+        }
+      }
+    }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------- top-k groups
     // Group tg owns queries tg*QPT .. tg*QPT+QPT-1 of each query tile (of
@@ -1635,7 +1739,8 @@ dsa_status run_score(dsa_ctx* ctx, const CUtensorMap& tq, const CUtensorMap& tk,
   auto kern = score_kernel<QT, FMT, KSEL, NQ>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return DSA_ERR_CUDA;
-  LaunchScope scope(ctx, FMT == DSA_FMT_BF16 ? DSA_K_SCORE_BF16 : DSA_K_SCORE_FP8, stream);
+  LaunchScope scope(ctx, FMT == DSA_FMT_BF16 ? DSA_K_SCORE_BF16 : FMT == DSA_FMT_FP8 ? DSA_K_SCORE_FP8 : DSA_K_SCORE_FP4,
+                    stream);
   const cudaError_t e = launch_pdl(kern, dim3(G), dim3(C::NTHREADS), C::SMEM, stream, tq, tk, args);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
@@ -1655,7 +1760,7 @@ dsa_status run_score_k(dsa_ctx* ctx, int k, const CUtensorMap& tq, const CUtenso
 int max_sequences() { return kMaxSeqs; }
 
 size_t topk_workspace(const dsa_ctx* ctx, int32_t Tq, int32_t B, int32_t k, dsa_fmt fmt) {
-  (void)fmt;  // the same for both cache formats
+  (void)fmt;  // the same for every cache format
   return ws_layout(ctx->num_sms, Tq, B, select_size(k), ctx->hadamard != 0).total;
 }
 
@@ -1712,6 +1817,8 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return DSA_ERR_CUDA;
+  } else if (fmt == DSA_FMT_FP4) {
+    tk = tq;  // fp4 codes come by plain bulk copies: no tensor map (the argument goes unused)
   } else {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), 64, static_cast<cuuint64_t>(num_pages)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPageBytesFp8)};
@@ -1741,14 +1848,17 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   const int G = L.G;
   dsa_status st;
   if (ctx->hadamard)  // one-query tiles (pick_qt), one more query term
-    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream)
-                             : run_score_k<1, DSA_FMT_FP8, 3>(ctx, ksel, tq, tk, args, G, stream);
+    st = fmt == DSA_FMT_BF16  ? run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream)
+         : fmt == DSA_FMT_FP8 ? run_score_k<1, DSA_FMT_FP8, 3>(ctx, ksel, tq, tk, args, G, stream)
+                              : run_score_k<1, DSA_FMT_FP4, 3>(ctx, ksel, tq, tk, args, G, stream);
   else if (L.QT == 4)
-    st = fmt == DSA_FMT_BF16 ? run_score_k<4, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
-                             : run_score_k<4, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+    st = fmt == DSA_FMT_BF16  ? run_score_k<4, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
+         : fmt == DSA_FMT_FP8 ? run_score_k<4, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream)
+                              : run_score_k<4, DSA_FMT_FP4, 2>(ctx, ksel, tq, tk, args, G, stream);
   else
-    st = fmt == DSA_FMT_BF16 ? run_score_k<1, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
-                             : run_score_k<1, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+    st = fmt == DSA_FMT_BF16  ? run_score_k<1, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream)
+         : fmt == DSA_FMT_FP8 ? run_score_k<1, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream)
+                              : run_score_k<1, DSA_FMT_FP4, 2>(ctx, ksel, tq, tk, args, G, stream);
   return st;
 }
 

@@ -86,7 +86,7 @@ extern "C" dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const f
                                             int32_t* out_idx, float* out_score,
                                             dsa_stream_t stream) {
   if (!ctx) return DSA_ERR_INVALID_ARG;
-  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8) return DSA_ERR_UNSUPPORTED;
+  if (fmt != DSA_FMT_BF16 && fmt != DSA_FMT_FP8 && fmt != DSA_FMT_FP4) return DSA_ERR_UNSUPPORTED;
   if (k < 1 || k > 2048) return DSA_ERR_UNSUPPORTED;
   if (Tq < 0 || B <= 0 || max_pages <= 0 || num_pages <= 0) return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(num_pages) * 64 > 0x7FFFFFFFLL) return DSA_ERR_UNSUPPORTED;

@@ -13,7 +13,8 @@ import os
 
 FMT_BF16 = 0
 FMT_FP8 = 1
-KERNEL_KINDS = ("store", "plan", "score_bf16", "score_fp8")
+FMT_FP4 = 2
+KERNEL_KINDS = ("store", "plan", "score_bf16", "score_fp8", "score_fp4")
 HEADS = 64
 HEAD_DIM = 128
 PAGE_SIZE = 64

@@ -65,8 +65,16 @@ typedef enum {
 
 typedef enum {
   DSA_FMT_BF16 = 0, /* 128 bf16 per token = 256 B; page = [64][128] bf16 = 16384 B      [DEC] */
-  DSA_FMT_FP8 = 1   /* 128 e4m3 + 1 fp32 scale = 132 B per token; page = [64][128] e4m3
+  DSA_FMT_FP8 = 1,  /* 128 e4m3 + 1 fp32 scale = 132 B per token; page = [64][128] e4m3
                        followed by [64] fp32 scales = 8448 B                            [VAL] */
+  DSA_FMT_FP4 = 2   /* 128 e2m1 (OCP MX FP4: 1 sign, 2 exponent bits with bias 1, 1
+                       mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) packed two
+                       per byte, the even dimension in the low nibble, + 1 fp32 scale
+                       = 68 B per token; page = [64][64] code bytes followed by [64]
+                       fp32 scales = 4352 B. [DEC], section "The Message: A Blueprint
+                       for Kernel Modification", names an fp4 variant of the indexer
+                       kernel for more aggressive compression without a layout; this
+                       one is the fp8 key with its element type narrowed to e2m1. */
 } dsa_fmt;
 
 enum { DSA_HEADS = 64, DSA_HEAD_DIM = 128, DSA_PAGE_SIZE = 64 };
@@ -88,7 +96,7 @@ dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_
 /* Free the context's device memory. Synchronises the device first. */
 dsa_status dsa_ctx_destroy(dsa_ctx* ctx);
 
-/* Bytes per cache page for a format (16384 or 8448); 0 for an unknown format. */
+/* Bytes per cache page for a format (16384, 8448 or 4352); 0 for an unknown format. */
 size_t dsa_cache_page_bytes(dsa_fmt fmt);
 
 /* Index-key store ([VAL], [DEC]): for each token t,
@@ -96,7 +104,8 @@ size_t dsa_cache_page_bytes(dsa_fmt fmt);
  *   y' = RoPE(y, rope_pos[t])                 (dims i and i+64 rotated together)
  *   written to page page_table[seq_id[t]][rope_pos[t] / 64], slot rope_pos[t] % 64:
  *   bf16: round-to-nearest-even of y'; fp8: scale = max(max|y'|, 1e-4) / 448,
- *   e4m3 (round to nearest even, saturating) of y' * (1/scale), and the scale.
+ *   e4m3 (round to nearest even, saturating) of y' * (1/scale), and the scale;
+ *   fp4: the same with 6 for 448 and e2m1 for e4m3.
  * The fp32 operations follow one fixed order, so the stored bytes are
  * reproducible bit for bit (sum of squares: 16 sequential partials over 8
  * consecutive dims, then a pairwise tree; every product and sum of the
@@ -154,14 +163,18 @@ size_t dsa_index_topk_workspace_size(const dsa_ctx* ctx, int32_t Tq, int32_t B, 
  * cu_q[b] .. cu_q[b+1]-1, position p = seq_lens[b] - n_q(b) + j for the j-th),
  *   s[r, key] = sum_h head_w[r][h] * max(0, sum_d q[r][h][d] * k[key][d])
  * over the visible keys of sequence b: positions 0..p when causal, else
- * 0..seq_lens[b]-1; k is the stored key (fp8: e4m3 value times its scale).
+ * 0..seq_lens[b]-1; k is the stored key (fp8 / fp4: e4m3 / e2m1 value times
+ * its scale).
  * Output row r holds the positions (within the sequence) and fp32 scores of
  * the min(k, visible) best keys, ordered by (score desc, position asc);
  * unused slots are -1 / -inf. Products accumulate in fp32. For fp8 caches
  * the stored e4m3 keys enter the tensor cores as they are and each query row
  * (one head) as two e4m3 terms under a power-of-two scale: exact for every
  * query value of at least 2^-10 of its row's largest magnitude, smaller
- * values off by at most 2^-17 of that magnitude.
+ * values off by at most 2^-17 of that magnitude. fp4 caches take the same
+ * path: the scorer widens each tile's e2m1 codes to e4m3 in shared memory
+ * (exact: every e2m1 value is an e4m3 value), so only the bytes read from
+ * memory shrink.
  *  q           (device) [Tq][64][128] bf16, 16-byte aligned.
  *  head_w      (device) [Tq][64] fp32, 16-byte aligned.
  *  cache       (device) as written by dsa_index_store, num_pages pages of fmt.
@@ -224,7 +237,8 @@ typedef enum {
   DSA_K_PLAN = 1,       /* dsa_index_topk: schedule */
   DSA_K_SCORE_BF16 = 2, /* dsa_index_topk: tensor-core scorer + running top-k, bf16 cache */
   DSA_K_SCORE_FP8 = 3,  /* the same, fp8 cache */
-  DSA_K_COUNT = 4
+  DSA_K_SCORE_FP4 = 4,  /* the same, fp4 cache */
+  DSA_K_COUNT = 5
 } dsa_kernel_kind;
 dsa_status dsa_profile_enable(dsa_ctx* ctx, int on);
 dsa_status dsa_profile_read(dsa_ctx* ctx, float* ms /* [DSA_K_COUNT] */,

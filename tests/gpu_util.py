@@ -98,14 +98,15 @@ def compare_all_rows(wl, fmt, cache, gi, gs, rows=None, k=None, block=1024, hada
 
 
 def slot_bytes(cache_np: np.ndarray, fmt: int, wl, pos, seq):
-    """Bytes of the given tokens' slots (data + scale for fp8), [n, token_bytes]."""
+    """Bytes of the given tokens' slots (codes + scale for fp8 / fp4), [n, token_bytes]."""
     page, off = S.slots(pos, seq, wl.page_table, wl.num_pages)
     pb = S.PAGE_BYTES[fmt]
     if fmt == S.FMT_BF16:
         base = page * pb + off * 256
         return cache_np[base[:, None] + np.arange(256)[None, :]]
-    base = page * pb + off * 128
-    data = cache_np[base[:, None] + np.arange(128)[None, :]]
-    sb = page * pb + 8192 + off * 4
+    cb = S.CODE_BYTES[fmt]
+    base = page * pb + off * cb
+    data = cache_np[base[:, None] + np.arange(cb)[None, :]]
+    sb = page * pb + 64 * cb + off * 4
     sc = cache_np[sb[:, None] + np.arange(4)[None, :]]
     return np.concatenate([data, sc], axis=1)

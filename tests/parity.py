@@ -9,7 +9,9 @@ Acceptance per query row:
     swap_tol * max|s| of the oracle's k-th score (max|s| over the row's
     visible keys);
   * logits: max |gpu score - oracle score at the same position| divided by
-    max |oracle top-k score| is at most logit_tol (2e-3 bf16, 3e-2 fp8).
+    max |oracle top-k score| is at most logit_tol (2e-3 bf16, 3e-2 fp8 and
+    fp4: the fp4 keys are widened to e4m3 exactly, so their scores carry the
+    same query-side rounding as fp8 keys).
 """
 from __future__ import annotations
 
@@ -18,7 +20,7 @@ import dataclasses
 import numpy as np
 
 SWAP_TOL = 1e-3
-LOGIT_TOL = {0: 2e-3, 1: 3e-2}
+LOGIT_TOL = {0: 2e-3, 1: 3e-2, 2: 3e-2}
 
 
 @dataclasses.dataclass

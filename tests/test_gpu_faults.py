@@ -65,7 +65,7 @@ def test_bounded_wait_reports_timeout_and_context_stays_usable(ctx):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 @pytest.mark.parametrize("shape", ["decode", "prefill"])
 def test_no_writes_outside_buffers(ctx, fmt, shape):
     import torch
@@ -134,7 +134,7 @@ def test_wrong_device_rejected_without_launch():
         c.close()
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 @pytest.mark.parametrize("shape", ["decode", "prefill"])
 def test_scorer_skips_out_of_range_page(ctx, fmt, shape):
     # the keys are stored through a valid page table; top-k then reads a copy

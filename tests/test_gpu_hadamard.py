@@ -33,7 +33,7 @@ def _oracle_cache(wl, fmt):
     return c
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_rotated_store_bitexact(ctx, fmt):
     rng = np.random.default_rng(31)
     T = 700
@@ -55,7 +55,7 @@ def test_rotated_store_bitexact(ctx, fmt):
     assert len(bad) == 0, f"{len(bad)} tokens differ, first at token {bad[0]}"
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 @pytest.mark.parametrize("case", ["prefill", "decode"])
 def test_rotated_topk_parity(ctx, fmt, case):
     if case == "prefill":

@@ -29,7 +29,7 @@ def _compare_cache(wl, fmt, d, pos, seq):
     assert len(bad) == 0, f"{len(bad)} tokens differ, first at token {bad[0]}"
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_store_bitexact_small(ctx, fmt):
     wl = I.make_workload("st", [300, 777, 129, 64, 1], [1] * 5, [300, 777, 129, 64, 1], True, 512,
                          seed=21, wid=20)
@@ -40,11 +40,11 @@ def test_store_bitexact_small(ctx, fmt):
     got = d["cache"].cpu().numpy()
     page = int(wl.page_table[0, 4])
     pb = S.PAGE_BYTES[fmt]
-    tb = 256 if fmt == S.FMT_BF16 else 128
+    tb = 256 if fmt == S.FMT_BF16 else S.CODE_BYTES[fmt]
     assert np.all(got[page * pb + 44 * tb: page * pb + 64 * tb] == 0)
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_store_bitexact_extreme_values(ctx, fmt):
     # wide dynamic range, zero rows, tiny rows, rows with one huge element
     rng = np.random.default_rng(5)
@@ -62,14 +62,14 @@ def test_store_bitexact_extreme_values(ctx, fmt):
     _compare_cache(wl, fmt, d, wl.new_pos, wl.new_seq)
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_store_bitexact_tiny_prefill(ctx, fmt):
     wl = I.tiny_prefill()
     d = U.device_workload(wl, fmt, ctx, store_fill=False)
     _compare_cache(wl, fmt, d, wl.new_pos, wl.new_seq)
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 def test_store_bitexact_long_positions(ctx, fmt):
     # the long-decode append: 8 sequences x 256 tokens at positions 130816..131071
     wl = I.make_workload("ap", [131072] * 8, [1] * 8, [256] * 8, True, 1024, seed=0, wid=4)

@@ -19,7 +19,7 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [S.FMT_BF16, S.FMT_FP8]
+FMTS = [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4]
 
 
 @functools.lru_cache(maxsize=None)

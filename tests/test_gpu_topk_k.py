@@ -46,14 +46,14 @@ def _prefill():
     return I.make_workload("kp", [3300, 260], [260, 120], [3300, 260], True, 512, seed=43, wid=42)
 
 
-@pytest.mark.parametrize("k", [1, 100, 700, 1500, 2048])
+@pytest.mark.parametrize("k,fmt", [(1, S.FMT_BF16), (100, S.FMT_FP8), (700, S.FMT_FP4), (1500, S.FMT_FP8),
+                                   (2048, S.FMT_BF16), (2048, S.FMT_FP4)])
 @pytest.mark.parametrize("shape", ["decode", "prefill"])
-def test_any_k(ctx, shape, k):
+def test_any_k(ctx, shape, k, fmt):
     # k above 1024 runs the top-2048 selection (in one-query tiles, for the
     # prefill shape too); the contexts here are long enough that 2048 of the
     # visible keys are selected, not all of them
     wl = _decode() if shape == "decode" else _prefill()
-    fmt = S.FMT_BF16 if k not in (100, 1500) else S.FMT_FP8
     d = U.device_workload(wl, fmt, ctx)
     gi, gs = U.run_topk(wl, fmt, ctx, d, k)
     assert ctx.device_status() == 0

@@ -34,7 +34,7 @@ def _call_static(ctx, wl, fmt, d, k, out_i, out_s):
     return st
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_static_scratch_matches_workspace_path(fmt):
     import torch
     from dsa_sparse_attention_store_gb300 import Context
