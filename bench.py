@@ -44,8 +44,8 @@ if ROOT not in sys.path:
 METRIC = "indexer queries/s and key-scores/s (bf16 & fp8) + % of HBM/TC roofline"
 HEADLINE = "long_prefill"
 WORKLOAD_NAMES = ["tiny_prefill", "batched_decode", "long_prefill", "needle", "long_decode"]
-FMT_NAMES = {0: "bf16", 1: "fp8"}
-TOKEN_BYTES = {0: 256, 1: 132}
+FMT_NAMES = {0: "bf16", 1: "fp8", 2: "fp4"}
+TOKEN_BYTES = {0: 256, 1: 132, 2: 68}
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CSRC = os.path.join(ROOT, "dsa_sparse_attention_store_gb300", "csrc")
@@ -78,7 +78,8 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms: float
 
 def scorer_algorithmic(wl, fmt: int):
     """(bytes, flops) one scorer launch must move / do for workload wl in
-    cache format fmt: every visible key read once (256 B bf16, 132 B fp8),
+    cache format fmt: every visible key read once (256 B bf16, 132 B fp8,
+    68 B fp4),
     the queries (16 KB each, bf16 or two e4m3 terms) and head weights, one
     4-byte page id per page, 8 bytes per output entry; 2 * 64 * 128 flops
     per (query, visible key) pair."""
@@ -92,7 +93,7 @@ def scorer_algorithmic(wl, fmt: int):
 
 def store_algorithmic(tokens: int, fmt: int) -> int:
     """Bytes one store launch must move for `tokens` tokens: the 256-byte raw
-    key read, the 256 (bf16) or 132 (fp8) bytes written, and the token's
+    key read, the 256 (bf16), 132 (fp8) or 68 (fp4) bytes written, and the token's
     position and sequence id (8 bytes). The RoPE table row (512 B) and the
     page id are not counted: they repeat across tokens and sequences."""
     return tokens * (256 + TOKEN_BYTES[fmt] + 8)
@@ -109,6 +110,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-store-roofline", action="store_true")
+    ap.add_argument("--no-fp4", action="store_true", help="skip the fp4-cache figures")
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle seconds per workload")
     return ap.parse_args(argv)
 
@@ -168,7 +170,7 @@ def workload_config(wl, name, fmts):
         "key_scores_per_step": int(wl.key_scores() * len(fmts)),
         "k": wl.k,
         "causal": wl.causal,
-        "l2": "flushed between timed steps (256 MB write, outside the timed events)",
+        "l2": "flushed between timed steps (256 MB write, then 256 MB read of another buffer; outside the timed events)",
     }
 
 
@@ -236,20 +238,22 @@ def build_lib():
 def roofline_entry(kind, avg_ms, nbytes, flops, fmt, peaks, peak_src, traffic, launches):
     """The binding roofline of one kernel: HBM bytes or tensor flops, which
     ever needs more time at its peak. The fp8 scorer's contraction is
-    e4m3 x e4m3 (two query terms per key), so its tensor peak is the fp8
-    one: the measured bf16 peak times the nominal fp8/bf16 ratio."""
+    e4m3 x e4m3 (two query terms per key), and so is the fp4 scorer's (its
+    keys widened to e4m3 on chip), so their tensor peak is the fp8 one: the
+    measured bf16 peak times the nominal fp8/bf16 ratio."""
+    e8 = fmt in (1, 2)
     hbm = nbytes / (avg_ms / 1e3) / 1e9
     out = {"kernel": kind, "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": avg_ms,
            "launches": launches, "traffic": traffic}
     if flops:
         tc = flops / (avg_ms / 1e3) / 1e12
-        tpk = peaks["bf16_tflops"] * (FP8_PER_BF16 if fmt == 1 else 1.0)
-        tpk_s = peaks.get("bf16_tflops_sustained", tpk) * (FP8_PER_BF16 if fmt == 1 else 1.0)
+        tpk = peaks["bf16_tflops"] * (FP8_PER_BF16 if e8 else 1.0)
+        tpk_s = peaks.get("bf16_tflops_sustained", tpk) * (FP8_PER_BF16 if e8 else 1.0)
         out["algorithmic_flops_per_launch"] = flops
-        if fmt == 1:
+        if e8:
             out["executed_tensor_flops_per_launch"] = 2 * flops
         if tc / tpk > hbm / peaks["hbm_gbs"]:
-            dt = "fp8 (e4m3; measured bf16 x nominal 2)" if fmt == 1 else "bf16"
+            dt = "fp8 (e4m3; measured bf16 x nominal 2)" if e8 else "bf16"
             out.update({"bound": "tensor", "achieved": tc, "peak": tpk, "unit": "TFLOP/s", "frac": tc / tpk,
                         "frac_of_sustained_peak": tc / tpk_s,
                         "peak_source": f"{peak_src} dense {dt} burst"})
@@ -415,7 +419,46 @@ def measure_workload(name, args, ctx, dev, world, barrier, flush, peaks, peak_sr
         out["e2e"] = {"value": whole_job_rate(ks_step, args.steps, world, e2e_ms), "unit": "key-scores/s",
                       "h2d_bytes_per_step": dv.h2d_bytes(), "d2h_bytes_per_step": dv.d2h_bytes(),
                       "ms_per_step": e2e_ms / args.steps}
+    if not args.no_fp4:
+        out["fp4"] = measure_fp4(wl, name, args, ctx, dev, world, barrier, flush, peaks, peak_src)
     return out, wl, fmts, dv
+
+
+def measure_fp4(wl, name, args, ctx, dev, world, barrier, flush, peaks, peak_src):
+    """The same workload on an fp4 cache alone (store + top-k per step): its
+    throughput and scorer roofline. Not part of the headline step, whose
+    formats are the pages' bf16 and fp8."""
+    import torch
+    dv = Device(wl, [2], ctx, dev)
+    for _ in range(args.warmup):
+        dv.step()
+        flush()
+    ctx.profile_read()
+    barrier()
+    step_ms = timed(dv.step, args.steps, flush)
+    barrier()
+    total_ms = sum(step_ms)
+    ctx.profile_read()                      # only the profiled steps below count
+    ctx.profile_enable(True)
+    for _ in range(args.steps):
+        dv.step()
+        flush()
+    torch.cuda.synchronize()
+    ctx.profile_enable(False)
+    prof = ctx.profile_read()
+    st = ctx.device_status()
+    if st != 0:
+        raise RuntimeError(f"{name} fp4: device status {st}")
+    if world > 1:
+        (total_ms,) = max_over_ranks([total_ms], dev)
+    sc_ms, sc_n = prof["score_fp4"]
+    nbytes, flops = scorer_algorithmic(wl, 2)
+    del dv
+    return {"value": whole_job_rate(wl.key_scores(), args.steps, world, total_ms), "unit": "key-scores/s",
+            "ms_per_step": total_ms / args.steps,
+            "kernel_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+            "roofline": roofline_entry("score_kernel (fp4 cache)", sc_ms / max(sc_n, 1), nbytes, flops, 2,
+                                       peaks, peak_src, traffic_of(f"{name}/score/fp4", scorer_hash()), sc_n)}
 
 
 def store_roofline(dv, which, args, flush, peaks, peak_src, label):
@@ -456,9 +499,14 @@ def run_ours(args, rank, world, local_rank):
     ctx = Context(theta=10000.0, eps=1e-6, max_pos=131072)
     peaks, peak_src = load_peaks()
     l2 = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    l2r = torch.ones(256 << 20, dtype=torch.uint8, device=dev).view(torch.int64)
 
     def flush():
+        # write a buffer larger than L2, then read another one: no input of
+        # the next step is left in L2, and no dirty line of the flush is left
+        # for the timed step to write back
         l2.fill_(1)
+        torch.sum(l2r)
 
     dist = world > 1
     if dist:
@@ -598,6 +646,7 @@ def compose(args, world, results, stores, wls, clocks):
         "kernel_ms_per_step": h["kernel_ms_per_step"],
         "roofline": roof[first],
         "roofline_other_format": roof.get("fp8") if first == "bf16" else None,
+        "roofline_fp4": h["fp4"]["roofline"] if "fp4" in h else None,
         "gpu_launches": h["gpu_launches"],
         "launches_per_step": h["launches_per_step"],
         "clocks": clocks,
