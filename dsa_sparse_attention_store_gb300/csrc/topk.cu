@@ -463,16 +463,16 @@ struct Cfg {
   static constexpr int QPT = ALT ? 1 : QT / NTK;         // queries per top-k group
   static constexpr int NBUF = ALT ? 2 : QT;              // running top-k buffers
   // key-tile operand stages (32 KB bf16, 16 KB e4m3): enough bytes in flight
-  // per SM to cover the HBM latency of a streaming one-query tile
-  // (four-query tiles selecting 1024 keys trade a stage for a candidate
-  // buffer twice the selection: a smaller buffer would select every tile)
+  // per SM to cover the HBM latency of a streaming one-query tile; the
+  // four-query tiles of a prefill read their keys from L2 and keep two bf16
+  // stages (a third measured 1 % slower on the 22528-token prefill)
   // fp4 keys: the tile's e2m1 codes land in a ring of their own (NR slots
   // of 8 KB, the bytes in flight) and the converter warps widen them into
   // an operand stage, which then only has to cover the conversion and MMA
   static constexpr bool FP4 = FMT == DSA_FMT_FP4;
   static constexpr bool E8 = FMT != DSA_FMT_BF16;        // e4m3 operands (fp8, or widened fp4)
   static constexpr int S = FP4 ? (QT == 4 ? 2 : 3)
-                               : QT == 4 ? (FMT == DSA_FMT_BF16 ? (KSEL > 512 ? 2 : 3) : (KSEL > 512 ? 4 : 6))
+                               : QT == 4 ? (FMT == DSA_FMT_BF16 ? 2 : (KSEL > 512 ? 4 : 6))
                                          : (FMT == DSA_FMT_BF16 ? 4 : 6);
   static constexpr int NR = FP4 ? (QT == 4 ? 3 : 6) : 0;  // raw fp4 tile slots
   static constexpr int RAW_BYTES = kTile * 64;
@@ -550,7 +550,7 @@ struct Misc {
   int gok[4], glast[4], gdigit[4], gabove[4], gcd[4];  // per top-k group
   int wsum[4][2][4];
   unsigned long long gmin[4][4], gmax[4][4];
-  unsigned int hmax[4];  // per buffer: largest score word pushed in the query tile
+  unsigned int hmax[4];  // per top-k group: largest candidate score word, for a cut
 };
 static_assert(sizeof(Misc) <= 2048, "misc");
 
@@ -813,25 +813,36 @@ __device__ void group_compact(uint64_t* buf, int* cnt, unsigned long long* thr, 
 
 // Cut buf[0..n) back, cheaply, to the keys of the top score bins holding at
 // least K keys, once a threshold is known: every key lies above the current
-// threshold, so the high words (ordered scores) span thr_hi .. hmax; 256
-// bins of a power-of-two width cover that span, one histogram finds the bin
-// B that holds the K-th largest key, and the keys of bins >= B stay: K ..
-// K + |B| of them. The threshold rises to just below bin B's lower edge,
-// which is at most the K-th largest key, so no key of the top K is lost.
-// Two passes over the buffer (histogram, compaction) where the exact radix
-// select takes six to eight. Returns false, leaving the buffer as it is,
+// threshold, so the high words (ordered scores) span thr_hi .. hmax (the
+// largest, found by a first pass); 256 bins of a power-of-two width cover
+// that span, one histogram finds the bin B that holds the K-th largest key,
+// and the keys of bins >= B stay: K .. K + |B| of them. The threshold rises
+// to just below bin B's lower edge, which is at most the K-th largest key,
+// so no key of the top K is lost. Three passes over the buffer (maximum,
+// histogram, compaction) where the exact radix select takes six to eight. Returns false, leaving the buffer as it is,
 // when the cut would keep more than `room` keys. hist: 256 words.
-__device__ bool group_cut(uint64_t* buf, int* cnt, unsigned long long* thr, unsigned int hmax, int K,
-                          int room, uint32_t* hist, Misc* ms, int g, int gt, int barid) {
+__device__ bool group_cut(uint64_t* buf, int* cnt, unsigned long long* thr, int K, int room,
+                          uint32_t* hist, Misc* ms, int g, int gt, int barid) {
   const int n = *cnt;
   if (n <= K) return true;
   const int w = gt >> 5, lane = gt & 31;
   const uint32_t lo = static_cast<uint32_t>(*thr >> 32);
+  // the largest candidate's score word bounds the bins from above
+  if (gt == 0) ms->hmax[g] = 0u;
+  for (int i = gt; i < 256; i += 128) hist[i] = 0u;
+  uint32_t hm = 0u;
+  for (int i = gt; i < n; i += 128) {
+    const uint32_t h = static_cast<uint32_t>(buf[i] >> 32);
+    hm = h > hm ? h : hm;
+  }
+  hm = __reduce_max_sync(0xffffffffu, hm);
+  named_bar(barid, 128);
+  if (lane == 0) atomicMax(&ms->hmax[g], hm);
+  named_bar(barid, 128);
+  const uint32_t hmax = ms->hmax[g];
   if (hmax < lo) return false;
   const uint64_t span1 = static_cast<uint64_t>(hmax - lo);  // span - 1
   const int sh = span1 >= 256 ? (64 - __clzll(static_cast<long long>(span1))) - 8 : 0;
-  for (int i = gt; i < 256; i += 128) hist[i] = 0u;
-  named_bar(barid, 128);
   for (int i = gt; i < n; i += 128) {
     const uint32_t h = static_cast<uint32_t>(buf[i] >> 32);
     atomicAdd(&hist[(h - lo) >> sh], 1u);
@@ -1589,7 +1600,6 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
         if (gt == 0) {
           ms->cnt[jb] = 0;
           ms->thr[jb] = 0;
-          ms->hmax[jb] = 0u;
         }
         thr[jj] = 0;
         nsel[jj] = 0;
@@ -1609,8 +1619,6 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
             const uint64_t key = make_key(sc, pos);
             const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
             push_key(pass, key, qlist(jj), &ms->cnt[jb], lane);
-            const unsigned int hw = __reduce_max_sync(0xffffffffu, pass ? static_cast<unsigned int>(key >> 32) : 0u);
-            if (lane == 0 && hw) atomicMax(&ms->hmax[jb], hw);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->st_empty[st]);
@@ -1636,8 +1644,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           if (ms->cnt[jb] > limit - kTile) {
             // after the first (exact) selection the threshold bounds the
             // scores from below and the cheap cut usually suffices
-            if (nsel[jj] == 0 || !group_cut(qlist(jj), &ms->cnt[jb], &ms->thr[jb], ms->hmax[jb], KSEL,
-                                            limit - 2 * kTile, hist, ms, tg, gt, barid))
+            if (nsel[jj] == 0 || !group_cut(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, limit - 2 * kTile,
+                                            hist, ms, tg, gt, barid))
               group_compact(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
             ++nsel[jj];
             unsigned long long t_new = ms->thr[jb];
