@@ -38,6 +38,7 @@ def test_status_strings_and_page_bytes(L):
         assert dsaidx.status_str(s)
     assert L.dsa_cache_page_bytes(0) == 16384
     assert L.dsa_cache_page_bytes(1) == 8448
+    assert L.dsa_cache_page_bytes(2) == 4352    # 64 x (64 code bytes + 4-byte scale)
     assert L.dsa_cache_page_bytes(7) == 0
 
 
