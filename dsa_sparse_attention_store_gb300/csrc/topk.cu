@@ -42,9 +42,10 @@
 //                         (one-query tiles: two groups on alternate query
 //                         tiles; four-query tiles: one group per query);
 //                         then output (or, for a query tile split across
-//                         CTAs, a sorted partial list, merged by the piece
-//                         that finishes last; its pieces share a running
-//                         threshold per query)
+//                         CTAs, an unsorted partial top-k; the piece that
+//                         finishes last streams all of them through its
+//                         filter, selects and sorts once; the pieces share
+//                         a running threshold per query)
 //           Keys sit on the MMA's M dimension so each score thread owns one
 //           key (one TMEM lane) and reduces over heads in its own registers.
 #include <cuda_bf16.h>
@@ -64,6 +65,10 @@ constexpr int kD = 128;
 constexpr int kTile = 128;  // keys per MMA tile = 2 pages
 constexpr int kPageBytesFp8 = 64 * 128 + 64 * 4;
 constexpr int kPageBytesFp4 = 64 * 64 + 64 * 4;
+// a query tile split over at most this many CTAs merges its pieces' sorted
+// lists pairwise; one split over more (selecting more than 512 keys) selects
+// once over their union
+constexpr int kFewPieces = 4;
 
 // The work is split evenly in units: a query tile with n key tiles costs
 // n + ovh units, ovh standing for its fixed costs (query load, final merge
@@ -488,8 +493,9 @@ struct Cfg {
   // CTA's piece of a decode query usually needs one selection, at its end
   static constexpr int TK = ALT ? (FMT == DSA_FMT_BF16 && NQ == 2 ? 3072 : 4096) : (KSEL > 512 ? 2304 : 1280);
   // a selection keeps KSEL keys and the cut aims below TK - 2 tiles: both
-  // must leave room for at least one more tile
-  static_assert(TK >= KSEL + 2 * 128 + 128, "candidate buffer too small for the selection");
+  // must leave room for one more tile, and the merge of a split query's
+  // lists for four 128-key chunks
+  static_assert(TK >= KSEL + 4 * 128, "candidate buffer too small for the selection and the merge");
   static constexpr int W_SCORE = 2;                      // first score warp
   static constexpr int W_TOPK = W_SCORE + NSW;           // first top-k warp
   static constexpr int W_CONV = W_TOPK + 4 * NTK;          // first converter warp
@@ -993,12 +999,6 @@ __device__ __forceinline__ void net_sort(uint64_t (&v)[K / 128], uint64_t* xbuf,
   }
 }
 
-// Sort a bitonic sequence of K slots descending.
-template <int K>
-__device__ __forceinline__ void net_merge(uint64_t (&v)[K / 128], uint64_t* xbuf, int w, int lane, int barid) {
-#pragma unroll
-  for (int stride = K >> 1; stride > 0; stride >>= 1) net_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
-}
 
 // Sort buf[0..n) (n <= K, distinct keys) into buf[0..K) descending, 0 in
 // the slots past n. buf (at least K keys) is the exchange buffer.
@@ -1017,6 +1017,13 @@ __device__ __forceinline__ void sort_list(uint64_t* buf, int n, int gt, int bari
 #pragma unroll
   for (int e = 0; e < E; ++e) buf[w * PW + lane * E + e] = v[e];
   named_bar(barid, 128);
+}
+
+// Sort a bitonic sequence of K slots descending.
+template <int K>
+__device__ __forceinline__ void net_merge(uint64_t (&v)[K / 128], uint64_t* xbuf, int w, int lane, int barid) {
+#pragma unroll
+  for (int stride = K >> 1; stride > 0; stride >>= 1) net_stage<K>(v, 2 * K, stride, xbuf, w, lane, barid);
 }
 
 // L := the K largest keys of the sorted lists src(c), c = c0..c1 (global
@@ -1559,8 +1566,8 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     // filters the staged scores against each query's threshold into its
     // candidate buffer, bounds the buffer (radix select), and
     // at the end of the query tile leaves the sorted top-k in the first KSEL
-    // slots and writes the row (or publishes the sorted list of its piece of
-    // the keys and, if it is the last piece to finish, merges all pieces).
+    // slots and writes the row (or publishes the top-k of its piece of the
+    // keys and, if it is the last piece to finish, merges all pieces).
     const int tg = (warp - C::W_TOPK) >> 2;
     const int gt = threadIdx.x - 32 * (C::W_TOPK + 4 * tg);
     const int barid = 1 + tg;
@@ -1664,12 +1671,26 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
       if (stop) break;
 
       // ------------------------------------------------ finish the segment
+      // a split query tile's pieces: CTAs cf .. cl. With a few, each sorts
+      // its top-k and the last merges the sorted lists pairwise; with many,
+      // the last streams the unsorted lists through its filter and selects
+      // and sorts once (the pairwise merges would cost one merge per piece)
+      // (selections of 512 keys always merge pairwise: their merges are
+      // cheap, and a decode kernel is better off without the second path's
+      // code, which runs cold once per CTA)
+      const int cf = s.whole ? cta : owner_of(s.qstart + ovh, total, Ge);  // owner of key tile 0
+      const int cl = s.whole ? cta : owner_of(s.qend - 1, total, Ge);
+      const bool many = KSEL > 512 && cl - cf + 1 > kFewPieces;
 #pragma unroll
       for (int jj = 0; jj < C::QPT; ++jj) {
         const int jb = qbuf(jj);
         group_compact(qlist(jj), &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
         if (share && gt == 0 && qrow(jj) < s.nrows) atomicMax(gthr + s.row0 + qrow(jj), ms->thr[jb]);
-        if (qrow(jj) < s.nrows) sort_list<KSEL>(qlist(jj), min(ms->cnt[jb], KSEL), gt, barid);
+        // a whole query tile, or a piece of one split in few pieces, is
+        // sorted here (the few sorted lists are merged); the pieces of a
+        // query tile split in many go out unsorted
+        if ((s.whole || !many) && qrow(jj) < s.nrows)
+          sort_list<KSEL>(qlist(jj), min(ms->cnt[jb], KSEL), gt, barid);
       }
       if (s.whole) {
 #pragma unroll
@@ -1682,22 +1703,25 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
         }
       } else {
         // this CTA holds one piece of the query tile's keys: publish its
-        // sorted top-k; the last piece to finish merges all of them
+        // top-k (sorted or not, 0 in the slots past its count); the last
+        // piece to finish merges all of them
         const int slot = partial_slot(cta, s.qstart, total, Ge);
 #pragma unroll
         for (int jj = 0; jj < C::QPT; ++jj) {
           const int j = qrow(jj);
           if (j < s.nrows) {
             const uint64_t* L = qlist(jj);
+            const int n = ms->cnt[qbuf(jj)];
             unsigned long long* dst = partials + (static_cast<long long>(slot) * QT + j) * KSEL;
 #pragma unroll
-            for (int i = 0; i < KSEL / 128; ++i) dst[i * 128 + gt] = L[i * 128 + gt];
+            for (int i = 0; i < KSEL / 128; ++i) {
+              const int x = i * 128 + gt;
+              dst[x] = x < n ? L[x] : 0ull;
+            }
           }
         }
         __threadfence();
         named_bar(barid, 128);
-        const int cf = owner_of(s.qstart + ovh, total, Ge);  // owner of key tile 0
-        const int cl = owner_of(s.qend - 1, total, Ge);
         if (gt == 0) {
           // one counter per query tile and group (per query tile when the
           // groups alternate: its pieces may sit in either group)
@@ -1706,7 +1730,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           __threadfence();
         }
         named_bar(barid, 128);
-        if (ms->glast[tg]) {
+        if (ms->glast[tg] && !many) {
 #pragma unroll
           for (int jj = 0; jj < C::QPT; ++jj) {
             const int j = qrow(jj);
@@ -1716,6 +1740,45 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
               };
               uint64_t* L = qlist(jj);
               merge_lists<KSEL>(src_of, cf, cl, L, L, gt, barid);
+              const long long o = static_cast<long long>(s.row0 + j) * a.kout;
+              write_row<KSEL>(L, a.out_idx + o, a.out_score + o, a.kout, out_pt(s), gt);
+            }
+          }
+        } else if (KSEL > 512 && ms->glast[tg]) {
+          // The pieces' lists stream through the running top-k once more,
+          // filtered from the start by the shared threshold: it is at least
+          // every piece's k-th key, so each key of the query's top k is
+          // above it, and most of the pieces' keys are not. One selection
+          // and one sort follow.
+#pragma unroll
+          for (int jj = 0; jj < C::QPT; ++jj) {
+            const int j = qrow(jj), jb = qbuf(jj);
+            if (j < s.nrows) {
+              uint64_t* L = qlist(jj);
+              if (gt == 0) {
+                ms->cnt[jb] = 0;
+                ms->thr[jb] = __ldcg(gthr + s.row0 + j);
+              }
+              named_bar(barid, 128);
+              // four 128-key chunks at a time, with room for them made first
+              const int nchunk = (cl - cf + 1) * (KSEL / 512);
+#pragma unroll 1
+              for (int q = 0; q < nchunk; ++q) {
+                const int c = cf + q / (KSEL / 512), i0 = (q % (KSEL / 512)) * 4;
+                const unsigned long long* src =
+                    partials + (static_cast<long long>(partial_slot(c, s.qstart, total, Ge)) * QT + j) * KSEL;
+                uint64_t kv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) kv[e] = __ldcg(src + (i0 + e) * 128 + gt);
+                if (ms->cnt[jb] > C::TK - 4 * kTile)
+                  group_compact(L, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+                const unsigned long long th = ms->thr[jb];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) push_key(kv[e] > th, kv[e], L, &ms->cnt[jb], lane);
+                named_bar(barid, 128);
+              }
+              group_compact(L, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
+              sort_list<KSEL>(L, min(ms->cnt[jb], KSEL), gt, barid);
               const long long o = static_cast<long long>(s.row0 + j) * a.kout;
               write_row<KSEL>(L, a.out_idx + o, a.out_score + o, a.kout, out_pt(s), gt);
             }
