@@ -140,7 +140,7 @@ def source_hash(names) -> str:
 
 
 def scorer_hash() -> str:
-    return source_hash(("topk.cu", "ptx.cuh", "internal.cuh"))
+    return source_hash(("scorer.cuh", "topk.cu", "topk_fp8.cu", "topk_fp4.cu", "ptx.cuh", "internal.cuh"))
 
 
 def store_hash() -> str:

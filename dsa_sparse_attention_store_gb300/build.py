@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build", platform.machine())
 STAMP = os.path.join(BUILD, "lib.stamp")
 LIB = os.path.join(HERE, "libdsaidx.so")
-SOURCES = ["api.cu", "store.cu", "topk.cu", "topk_static.cu"]
+SOURCES = ["api.cu", "store.cu", "topk.cu", "topk_fp8.cu", "topk_fp4.cu", "topk_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -1,0 +1,15 @@
+// The scorer's fp8 kernel variants (see scorer.cuh and topk.cu).
+#include "scorer.cuh"
+
+namespace dsa {
+namespace sc {
+
+dsa_status score_fp8(dsa_ctx* ctx, int qt, int nq, int ksel, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const ScoreArgs& args, int G, cudaStream_t stream) {
+  if (nq == 3) return run_score_k<1, DSA_FMT_FP8, 3>(ctx, ksel, tq, tk, args, G, stream);
+  if (qt == 4) return run_score_k<4, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+  return run_score_k<1, DSA_FMT_FP8, 2>(ctx, ksel, tq, tk, args, G, stream);
+}
+
+}  // namespace sc
+}  // namespace dsa
