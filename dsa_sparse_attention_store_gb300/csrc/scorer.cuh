@@ -17,7 +17,6 @@
 namespace dsa {
 namespace sc {
 
-
 constexpr int kH = 64;
 constexpr int kD = 128;
 constexpr int kTile = 128;  // keys per MMA tile = 2 pages
