@@ -1592,7 +1592,10 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
                 uint64_t kv[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) kv[e] = __ldcg(src + (i0 + e) * 128 + gt);
-                if (ms->cnt[jb] > C::TK - 4 * kTile)
+                // the threshold is a true lower bound from the start, so the
+                // cheap cut serves until the final exact selection
+                if (ms->cnt[jb] > C::TK - 4 * kTile &&
+                    !group_cut(L, &ms->cnt[jb], &ms->thr[jb], KSEL, C::TK - 5 * kTile, hist, ms, tg, gt, barid))
                   group_compact(L, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
                 const unsigned long long th = ms->thr[jb];
 #pragma unroll
