@@ -1361,16 +1361,22 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
             stop = true;
             break;
           }
-          const uint2* src = reinterpret_cast<const uint2*>(sRaw + rs * C::RAW_BYTES);
-          uint8_t* dst = sOp + slot * C::OP_BYTES;
-#pragma unroll 4
-          for (int i = ct; i < kTile * 8; i += 32 * C::NCV) {
-            const int r = i >> 3, c = i & 7;
-            const uint2 w = src[i];  // row r, dims 16c .. 16c+15
+          // chunk i = ct + 64 j (j < 16): row r = ct / 8 + 8 j, chunk column
+          // c = ct % 8, so the swizzled column and the row phase are this
+          // thread's constants and every address is a fixed offset; all
+          // sixteen loads go out before the first conversion
+          constexpr int PER = kTile * 8 / (32 * C::NCV);
+          const uint2* src = reinterpret_cast<const uint2*>(sRaw + rs * C::RAW_BYTES) + ct;
+          uint8_t* dst = sOp + slot * C::OP_BYTES + (ct >> 3) * 128 + (((ct & 7) ^ ((ct >> 3) & 7)) << 4);
+          uint2 w[PER];
+#pragma unroll
+          for (int jj = 0; jj < PER; ++jj) w[jj] = src[jj * 32 * C::NCV];
+#pragma unroll
+          for (int jj = 0; jj < PER; ++jj) {
             uint4 o;
-            e2m1x8_to_e4m3(w.x, o.x, o.y);
-            e2m1x8_to_e4m3(w.y, o.z, o.w);
-            *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+            e2m1x8_to_e4m3(w[jj].x, o.x, o.y);
+            e2m1x8_to_e4m3(w[jj].y, o.z, o.w);
+            *reinterpret_cast<uint4*>(dst + jj * (32 * C::NCV / 8) * 128) = o;
           }
           // the stage is read by the tensor cores (async proxy)
           fence_proxy_async_smem();
