@@ -157,8 +157,9 @@ constexpr int kMaxSeqs = 16384;
 // is, one warp turns a (query, head) row of 128 values into its tensor-core
 // terms in place, each lane taking 4 consecutive values:
 //
-// fp8 caches: the stored e4m3 keys go to the tensor cores as they are
-// (kind::f8f6f4, e4m3 x e4m3, both operands of one type), so the row is
+// fp8 and fp4 caches: the e4m3 keys (stored, or widened from e2m1) go to the
+// tensor cores as they are (kind::f8f6f4, e4m3 x e4m3, both operands of one
+// type), so the row is
 // split into e4m3 terms whose sum is the query: a power-of-two scale 2^e
 // puts the row's largest magnitude in [2^7, 2^8); t1 = e4m3(2^e q),
 // t2 = e4m3(2^e q - t1) (t3 likewise), each difference exact in fp32. A
@@ -175,7 +176,7 @@ constexpr int kMaxSeqs = 16384;
 // between lanes l and l ^ (h/4)); the rotated values are sums of up to 128
 // bf16 values and carry more bits than one bf16 or two e4m3 terms hold, so
 // bf16 caches take hi = bf16(x) and lo = bf16(x - hi) (16 significant bits)
-// and fp8 caches three e4m3 terms (12 significant bits); w' carries a
+// and fp8 and fp4 caches three e4m3 terms (12 significant bits); w' carries a
 // further 2^-7 (the transform's gain 128 on the dot product).
 //
 // Terms follow one another in shared memory: a bf16 term as two 64-column
@@ -348,10 +349,11 @@ struct Cfg {
   static constexpr int OFF_ST = OFF_TOPK + NBUF * TK * 8;
   static constexpr int OFF_W = OFF_ST + NST * ST_BYTES;
   static constexpr int OFF_HIST = OFF_W + 2 * QT * 64 * 4;   // head weights, double-buffered
-  // fp8 key scales of one-query tiles: the 2 x 64 fp32 scales of a tile's two
-  // pages come into a ring of their own by bulk copy beside the codes (the
-  // score warps read them after the MMA has released the operand stage);
-  // four-query tiles are slow enough per tile to load them from global memory
+  // fp8 / fp4 key scales of one-query tiles: the 2 x 64 fp32 scales of a
+  // tile's two pages come into a ring of their own by bulk copy beside the
+  // codes (the score warps read them after the MMA has released the operand
+  // stage); four-query tiles load them from global memory a tile ahead (a
+  // ring for them measured no faster)
   static constexpr bool SCALE_RING = E8 && QT == 1;
   static constexpr int NSC = SCALE_RING ? 16 : 0;          // scale slots (tiles)
   static constexpr int OFF_SC = OFF_HIST + NTK * 512 * 4;  // after the radix-select histograms
@@ -1179,7 +1181,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
     // ---------------------------------------------------------- score warps
     // Warp w reads its 32 TMEM lanes (keys) of query j's 64 columns, frees
     // the accumulator as soon as they are in registers, reduces them to
-    // one score per key (ReLU, head weights, fp8 key scale) and stages the
+    // one score per key (ReLU, head weights, fp8 / fp4 key scale) and stages the
     // scores, -inf for keys that are masked or in an invalid page.
     const int j0 = ((warp - C::W_SCORE) >> 2) * C::QSW;  // this warp's first query
     const int q4 = warp & 3;
@@ -1220,7 +1222,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
       const int ring = C::ALT ? (seg_i & 1) : 0;
       int rq = ring ? rq1 : rq0;  // tiles staged so far in this ring
       // page id of this thread's key in tile tt (-1: past the sequence or
-      // out of range), and the fp8 key's scale; issued ahead of use so the
+      // out of range), and the fp8 / fp4 key's scale; issued ahead of use so the
       // global-memory latency overlaps earlier tiles (page ids two tiles
       // ahead, scales one tile ahead)
       auto page_of = [&](int tt) -> int {
@@ -1259,7 +1261,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           break;
         }
         tc_fence_after();
-        float rscale = 1.f;  // this key's fp8 scale, from the scale ring
+        float rscale = 1.f;  // this key's scale (fp8 / fp4), from the scale ring
         if constexpr (C::SCALE_RING) {
           const int ss = tile_seq % C::NSC, uss = tile_seq / C::NSC;
           if (!__all_sync(0xffffffffu, mbar_wait(&ms->sc_full[ss], uss & 1))) {
