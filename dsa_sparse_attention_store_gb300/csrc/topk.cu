@@ -230,7 +230,11 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
   char* ws = static_cast<char*>(workspace);
   {
     LaunchScope scope(ctx, DSA_K_PLAN, stream);
-    const int ovh = L.QT == 4 ? 12 : 4;  // measured fixed cost of a query tile, in key tiles
+    // the fixed cost of a query tile, in key tiles (query load, final
+    // selection, sort and output); for four-query tiles swept on GB300 over
+    // 8..20: 14 balances the 22528- and 10498-token prefills (the longer one
+    // prefers more, the shorter less)
+    const int ovh = L.QT == 4 ? 14 : 4;
     // the prefix of the query tiles' costs stays in shared memory when it fits
     const size_t base = static_cast<size_t>(3 * B + 2) * sizeof(int);
     const size_t pre = static_cast<size_t>(L.qtmax + 1) * sizeof(long long);
