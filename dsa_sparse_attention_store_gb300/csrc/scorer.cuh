@@ -477,14 +477,19 @@ struct SegIter {
 // to PW use shuffles, larger ones (between warps) go through a K-key
 // shared-memory exchange buffer.
 
-__device__ __forceinline__ void push_key(bool pass, uint64_t key, uint64_t* buf, int* cnt, int lane) {
+__device__ __forceinline__ void push_key(bool pass, uint64_t key, uint64_t* buf, int* cnt, int cap,
+                                         unsigned int* status, int lane) {
   const unsigned m = __ballot_sync(0xffffffffu, pass);
   if (m) {
     const int leader = __ffs(m) - 1;
     int base = 0;
     if (lane == leader) base = atomicAdd(cnt, __popc(m));
     base = __shfl_sync(0xffffffffu, base, leader);
-    if (pass) buf[base + __popc(m & ((1u << lane) - 1u))] = key;
+    // the callers make room before every push; a key that would still land
+    // past the buffer is dropped and the overflow recorded, never written
+    if (lane == leader && base + __popc(m) > cap) atomicOr(status, DSA_DEV_BOUNDS);
+    const int idx = base + __popc(m & ((1u << lane) - 1u));
+    if (pass && idx < cap) buf[idx] = key;
   }
 }
 
@@ -1455,7 +1460,7 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
             const float sc = sSt[st * (QT * kTile) + j * kTile + gt];
             const uint64_t key = make_key(sc, pos);
             const bool pass = __float_as_uint(sc) != 0xff800000u && key > thr[jj];
-            push_key(pass, key, qlist(jj), &ms->cnt[jb], lane);
+            push_key(pass, key, qlist(jj), &ms->cnt[jb], C::TK, a.status, lane);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ms->st_empty[st]);
@@ -1478,6 +1483,11 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           // piece's last selection) small
           constexpr int kFirst = 2 * KSEL < C::TK ? 2 * KSEL : C::TK;
           const int limit = (C::ALT && nsel[jj] == 0) ? kFirst : C::TK;
+          if (ms->cnt[jb] > C::TK) {  // only after a recorded overflow: the dropped keys are gone
+            named_bar(barid, 128);
+            if (gt == 0) ms->cnt[jb] = C::TK;
+            named_bar(barid, 128);
+          }
           if (ms->cnt[jb] > limit - kTile) {
             // after the first (exact) selection the threshold bounds the
             // scores from below and the cheap cut usually suffices
@@ -1607,8 +1617,12 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
                   group_compact(L, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
                 const unsigned long long th = ms->thr[jb];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) push_key(kv[e] > th, kv[e], L, &ms->cnt[jb], lane);
+                for (int e = 0; e < 4; ++e) push_key(kv[e] > th, kv[e], L, &ms->cnt[jb], C::TK, a.status, lane);
                 named_bar(barid, 128);
+                if (ms->cnt[jb] > C::TK) {  // only after a recorded overflow
+                  if (gt == 0) ms->cnt[jb] = C::TK;
+                  named_bar(barid, 128);
+                }
               }
               group_compact(L, &ms->cnt[jb], &ms->thr[jb], KSEL, hist, ms, tg, gt, barid);
               sort_list<KSEL>(L, min(ms->cnt[jb], KSEL), gt, barid);

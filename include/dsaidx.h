@@ -58,7 +58,9 @@ typedef enum {
   DSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer ... */
   DSA_ERR_UNSUPPORTED = 2,   /* k not in 1..2048, unknown format, no sm_103 device */
   DSA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
-  DSA_ERR_DEVICE_BOUNDS = 4, /* device saw a page id / position / sequence out of range */
+  DSA_ERR_DEVICE_BOUNDS = 4, /* device saw a page id / position / sequence out of range (or a
+                                top-k candidate buffer would have overflowed: the keys are
+                                dropped, never written past the buffer) */
   DSA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
   DSA_ERR_WORKSPACE = 6      /* workspace too small */
 } dsa_status;
