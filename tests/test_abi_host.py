@@ -60,6 +60,10 @@ def test_invalid_arguments_rejected_without_device(L):
     assert L.dsa_index_store(fake, good, good, good, good, 1, 1, 1, P(0x100010), 1, 0, None) == 1
     # T == 0 is a no-op
     assert L.dsa_index_store(fake, None, None, None, None, 0, 1, 1, None, 1, 0, None) == 0
+    # and so is Tq == 0 (no buffer is needed, every format)
+    for f in (0, 1, 2):
+        empty = [None, None, None, 1, f, None, 1, None, None, 1, 0, 1]
+        assert L.dsa_index_topk(fake, *empty, 512, None, None, None, 0, None) == 0
     args = [good, good, good, 1, 0, good, 1, good, good, 1, 4, 1]
     # k above 2048
     assert L.dsa_index_topk(fake, *args, 2049, good, good, good, 1 << 30, None) == 2
