@@ -464,12 +464,14 @@ struct SegIter {
 
 // ------------------------------------------------------------------ running top-k (one group of 128 threads)
 // Keys above a query's threshold are appended to a shared-memory candidate
-// buffer as tiles arrive. A full buffer is cut back to its K largest keys by
-// a radix select, whose K-th key becomes the threshold; at the end of the
-// query tile the buffer is cut back once more and the K keys are sorted.
-// The buffer is large next to K, so the selections are few: one-query tiles
-// (decode) have one 4096-key buffer per group and a CTA's piece of a decode
-// query usually needs a single selection, at its end.
+// buffer as tiles arrive. A full buffer is cut back: the first time to its K
+// largest keys by an exact radix select, whose K-th key becomes the
+// threshold, later by a two-pass cut that keeps the score bins holding the
+// K largest and raises the threshold to their lower edge; at the end of the
+// query tile one exact selection leaves the K keys, which are sorted. The
+// buffer is large next to K, so the selections are few: one-query tiles
+// (decode) have one 3072- or 4096-key buffer per group and a CTA's piece of
+// a decode query usually needs one or two selections.
 //
 // The sorting networks run in registers over K slots held by the group's 4
 // warps: slot x = w*PW + lane*E + e is register e of lane `lane` of warp w
