@@ -65,10 +65,10 @@ def test_any_k(ctx, shape, k, fmt):
     assert ok, P.summary(reps)
 
 
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
 @pytest.mark.parametrize("shape", ["decode", "prefill"])
-def test_slot_output(ctx, ctx_slots, shape):
+def test_slot_output(ctx, ctx_slots, shape, fmt):
     wl = _decode() if shape == "decode" else _prefill()
-    fmt = S.FMT_BF16
     d = U.device_workload(wl, fmt, ctx)
     pi, ps = U.run_topk(wl, fmt, ctx, d)
     si, ss = U.run_topk(wl, fmt, ctx_slots, d)
