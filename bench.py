@@ -13,14 +13,18 @@ reported under "configs". Every workload carries its throughput with inputs
 resident, the end-to-end figure through the C ABI from pinned host buffers,
 the roofline of its scorer launches and the C++ oracle's CPU baseline; the
 store kernel's roofline is measured on the long decode's 1.05M-token fill and
-on the long prefill's 22528 tokens.
+on the long prefill's 22528 tokens. Each workload also reports the fp4 cache
+on its own ("fp4"), and the long prefill and the batched decode the options
+past the pages' path ("variants": the Hadamard-rotated cache, cache-slot
+output, and for the batched decode the top-2048 selection).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|NAME]
   python bench.py --impl reference ...   # the C++ oracle on a bounded sample
 
 Prints one JSON line. `value` is key-scores/s (sum over queries of the keys
 each query is scored against, both formats) over all GPUs; L2 is flushed
-(256 MB write) between timed steps, outside the timed events. `e2e` copies
+(256 MB write, then 256 MB read of another buffer) between timed steps,
+outside the timed events. `e2e` copies
 each step's inputs from pinned host memory and its top-k back inside the
 timed region. `roofline` is for the bf16 scorer of the headline workload,
 timed by the library's CUDA events on the launch stream.
@@ -111,6 +115,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-store-roofline", action="store_true")
     ap.add_argument("--no-fp4", action="store_true", help="skip the fp4-cache figures")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the Hadamard / k=2048 / slot-output figures")
     ap.add_argument("--cpu-seconds", type=float, default=6.0, help="oracle seconds per workload")
     return ap.parse_args(argv)
 
@@ -461,6 +467,59 @@ def measure_fp4(wl, name, args, ctx, dev, world, barrier, flush, peaks, peak_src
                                        peaks, peak_src, traffic_of(f"{name}/score/fp4", scorer_hash()), sc_n)}
 
 
+def measure_variant(wl, name, label, args, dev, world, barrier, flush, peaks, peak_src, hadamard=False,
+                    slots=False, k=None):
+    """One of the options past the pages' path on a workload, both formats
+    per step like the headline: the Hadamard-rotated cache and queries, the
+    top-2048 selection (k), or cache-slot output. Scorer rooflines of the
+    variant's own kernels (fresh context, so the store writes the rotated
+    keys when the rotation is on)."""
+    import copy
+    import torch
+    from dsa_sparse_attention_store_gb300 import Context
+    vwl = copy.copy(wl)
+    if k is not None:
+        vwl.k = k
+    ctx = Context(theta=10000.0, eps=1e-6, max_pos=131072)
+    try:
+        ctx.set_hadamard(hadamard)
+        ctx.set_slot_output(slots)
+        dv = Device(vwl, [0, 1], ctx, dev)
+        for _ in range(args.warmup):
+            dv.step()
+            flush()
+        ctx.profile_read()
+        barrier()
+        step_ms = timed(dv.step, args.steps, flush)
+        barrier()
+        total_ms = sum(step_ms)
+        ctx.profile_read()
+        ctx.profile_enable(True)
+        for _ in range(args.steps):
+            dv.step()
+            flush()
+        torch.cuda.synchronize()
+        ctx.profile_enable(False)
+        prof = ctx.profile_read()
+        st = ctx.device_status()
+        if st != 0:
+            raise RuntimeError(f"{name} {label}: device status {st}")
+        if world > 1:
+            (total_ms,) = max_over_ranks([total_ms], dev)
+        roofs = {}
+        for f in (0, 1):
+            sc_ms, sc_n = prof["score_" + FMT_NAMES[f]]
+            nbytes, flops = scorer_algorithmic(vwl, f)
+            roofs[FMT_NAMES[f]] = roofline_entry(f"score_kernel ({FMT_NAMES[f]} cache, {label})",
+                                                 sc_ms / max(sc_n, 1), nbytes, flops, f, peaks, peak_src,
+                                                 None, sc_n)
+        del dv
+        return {"value": whole_job_rate(vwl.key_scores() * 2, args.steps, world, total_ms),
+                "unit": "key-scores/s", "k": vwl.k, "ms_per_step": total_ms / args.steps, "roofline": roofs}
+    finally:
+        ctx.close()
+
+
 def store_roofline(dv, which, args, flush, peaks, peak_src, label):
     """Roofline of the store kernel on `which` tokens of a workload ('fill'
     or 'new'), one launch per timed iteration, per format."""
@@ -532,6 +591,16 @@ def run_ours(args, rank, world, local_rank):
         wls[name] = (wl, fmts)
         del dv
         torch.cuda.empty_cache()
+        if not args.no_variants and name in ("long_prefill", "batched_decode"):
+            var = {"hadamard": measure_variant(wl, name, "Hadamard", args, dev, world, barrier, flush, peaks,
+                                               peak_src, hadamard=True),
+                   "slots": measure_variant(wl, name, "slot output", args, dev, world, barrier, flush, peaks,
+                                            peak_src, slots=True)}
+            if name == "batched_decode":
+                var["k2048"] = measure_variant(wl, name, "k=2048", args, dev, world, barrier, flush, peaks,
+                                               peak_src, k=2048)
+            res["variants"] = var
+            torch.cuda.empty_cache()
     clocks = sampler.stop()
     ctx.close()
     return results, stores, wls, clocks
@@ -647,6 +716,7 @@ def compose(args, world, results, stores, wls, clocks):
         "roofline": roof[first],
         "roofline_other_format": roof.get("fp8") if first == "bf16" else None,
         "roofline_fp4": h["fp4"]["roofline"] if "fp4" in h else None,
+        "variants": h.get("variants"),
         "gpu_launches": h["gpu_launches"],
         "launches_per_step": h["launches_per_step"],
         "clocks": clocks,
