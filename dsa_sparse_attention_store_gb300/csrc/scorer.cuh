@@ -48,13 +48,15 @@ inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 constexpr int kMaxGrid = 1024;  // most CTAs of the scorer (one per SM)
 
-// Four-query tiles when the queries outnumber the sequences; one-query tiles
-// for decode, whenever the query carries more than the plain number of terms
-// (the Hadamard rotation), whose larger query tile only fits beside the
-// operand ring of a one-query tile, and for selections of 2048 keys, whose
-// candidate buffer only fits there.
+// Tiles of several queries of one sequence when the queries outnumber the
+// sequences: four, or two when the query carries one more term (the
+// Hadamard rotation), whose larger query tile only fits beside the operand
+// ring at half the width; one-query tiles for decode and for selections of
+// 2048 keys, whose candidate buffer only fits there.
 inline int pick_qt(int Tq, int B, bool hadamard, int ksel) {
-  return (!hadamard && ksel <= 1024 && Tq >= 2 * B && Tq >= 4) ? 4 : 1;
+  if (ksel > 1024 || Tq < 2 * B) return 1;
+  if (hadamard) return Tq >= 2 ? 2 : 1;
+  return Tq >= 4 ? 4 : 1;
 }
 // selection size (the sorting networks' K) for an output of k entries
 inline int select_size(int k) { return k <= 512 ? 512 : (k <= 1024 ? 1024 : 2048); }
@@ -301,7 +303,7 @@ struct Cfg {
   static constexpr bool E8 = FMT != DSA_FMT_BF16;        // e4m3 operands (fp8, or widened fp4)
   static constexpr int S = FP4 ? (QT == 4 ? 2 : 3)
                                : QT == 4 ? (FMT == DSA_FMT_BF16 ? 2 : (KSEL > 512 ? 4 : 6))
-                                         : (FMT == DSA_FMT_BF16 ? 4 : 6);
+                                         : (FMT == DSA_FMT_BF16 ? (QT == 2 ? 3 : 4) : 6);
   static constexpr int NR = FP4 ? (QT == 4 ? 3 : 6) : 0;  // raw fp4 tile slots
   static constexpr int RAW_BYTES = kTile * 64;
   static constexpr int NCV = FP4 ? 2 : 0;                 // converter warps
@@ -327,7 +329,7 @@ struct Cfg {
   // TMEM accumulator buffers: the MMA of a tile waits for the score warps
   // to have read the buffer it reuses, so a deeper ring hides that round
   // trip; four-query tiles fill the 512 columns with two
-  static constexpr int NTB = QT == 1 ? 4 : 2;
+  static constexpr int NTB = QT == 4 ? 2 : 4;
   static constexpr int TMEM_COLS = NTB * N;
   static constexpr int TERM_BYTES = N * 128 * (FMT == DSA_FMT_BF16 ? 2 : 1);  // one query term
   // a page: its key codes, then its 64 fp32 scales (e4m3 / e2m1 keys)

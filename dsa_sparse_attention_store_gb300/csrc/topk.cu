@@ -198,7 +198,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
 dsa_status score_bf16(dsa_ctx* ctx, int qt, int nq, int ksel, const CUtensorMap& tq, const CUtensorMap& tk,
                       const ScoreArgs& args, int G, cudaStream_t stream) {
-  if (nq == 2) return run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream);
+  if (nq == 2)
+    return qt == 2 ? run_score_k<2, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream)
+                   : run_score_k<1, DSA_FMT_BF16, 2>(ctx, ksel, tq, tk, args, G, stream);
   if (qt == 4) return run_score_k<4, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream);
   return run_score_k<1, DSA_FMT_BF16, 1>(ctx, ksel, tq, tk, args, G, stream);
 }
@@ -234,7 +236,7 @@ dsa_status launch_topk(dsa_ctx* ctx, const void* q, const float* head_w, const v
     // selection, sort and output); for four-query tiles swept on GB300 over
     // 8..20: 14 balances the 22528- and 10498-token prefills (the longer one
     // prefers more, the shorter less)
-    const int ovh = L.QT == 4 ? 14 : 4;
+    const int ovh = L.QT == 4 ? 14 : (L.QT == 2 ? 8 : 4);
     // the prefix of the query tiles' costs stays in shared memory when it fits
     const size_t base = static_cast<size_t>(3 * B + 2) * sizeof(int);
     const size_t pre = static_cast<size_t>(L.qtmax + 1) * sizeof(long long);

@@ -137,8 +137,9 @@ dsa_status dsa_index_store(dsa_ctx* ctx, const void* k_raw, const int32_t* rope_
  * meaning: (H q) . (H k) / 128 = q . k. The query is rotated exactly, as far
  * as the scores can tell: the fp32 rotation is carried as two bf16 terms
  * (hi + lo, 16 significant bits) for bf16 caches and three e4m3 terms (12
- * bits) for fp8 caches, each term its own pass of the tensor cores, and the
- * queries run in one-query tiles.
+ * bits) for fp8 and fp4 caches, each term its own pass of the tensor cores,
+ * and the queries run in tiles of two queries of one sequence (one for a
+ * decode batch, one query per sequence) instead of four.
  * A cache must be written and read with the same setting. Off by default;
  * applies to the calls made after it, and changes the size
  * dsa_index_topk_workspace_size reports. */
@@ -218,7 +219,7 @@ dsa_status dsa_index_topk(dsa_ctx* ctx, const void* q, const float* head_w, cons
  * dsa_index_topk_workspace_size(ctx, Tq, B, k, fmt) exceeds
  * DSA_STATIC_WORKSPACE_BYTES (on a 152-SM GB300 with one sequence: batches
  * up to about 1.29M queries with k <= 512 and 1.07M with 512 < k <= 1024,
- * either cache format; with the Hadamard rotation on, about 620K and 597K;
+ * any cache format; with the Hadamard rotation on, about 970K and 892K;
  * with k > 1024, about 549K, rotation on or off). */
 #define DSA_STATIC_WORKSPACE_BYTES (32u << 20)
 dsa_status dsa_index_topk_static(dsa_ctx* ctx, const void* q, const float* head_w,
