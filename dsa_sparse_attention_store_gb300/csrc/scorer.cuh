@@ -295,14 +295,15 @@ struct Cfg {
   // key-tile operand stages (32 KB bf16, 16 KB e4m3): enough bytes in flight
   // per SM to cover the HBM latency of a streaming one-query tile; the
   // four-query tiles of a prefill read their keys from L2 and keep two bf16
-  // stages (a third measured 1 % slower on the 22528-token prefill)
+  // stages (a third measured 1 % slower on the 22528-token prefill) or three
+  // e4m3 ones (six measured 2 % slower)
   // fp4 keys: the tile's e2m1 codes land in a ring of their own (NR slots
   // of 8 KB, the bytes in flight) and the converter warps widen them into
   // an operand stage, which then only has to cover the conversion and MMA
   static constexpr bool FP4 = FMT == DSA_FMT_FP4;
   static constexpr bool E8 = FMT != DSA_FMT_BF16;        // e4m3 operands (fp8, or widened fp4)
   static constexpr int S = FP4 ? (QT == 4 ? 2 : 3)
-                               : QT == 4 ? (FMT == DSA_FMT_BF16 ? 2 : (KSEL > 512 ? 4 : 6))
+                               : QT == 4 ? (FMT == DSA_FMT_BF16 ? 2 : 3)
                                          : (FMT == DSA_FMT_BF16 ? (QT == 2 ? 3 : 4) : 6);
   static constexpr int NR = FP4 ? (QT == 4 ? 3 : 6) : 0;  // raw fp4 tile slots
   static constexpr int RAW_BYTES = kTile * 64;
@@ -1292,21 +1293,22 @@ __global__ void __launch_bounds__(Cfg<QT, FMT, KSEL, NQ>::NTHREADS, 1)
           const uint32_t tl = tbase + (static_cast<uint32_t>(q4 * 32) << 16) +
                               static_cast<uint32_t>(buf * C::N + j * 64);
           const float4* w4 = reinterpret_cast<const float4*>(sWs + j * 64);
-          // two halves of 32 columns through one register buffer
-          float v[32];
+          // four quarters of 16 columns through one register buffer (32-column
+          // halves made the fp8 four-query scorer spill: 7 % slower)
+          float v[16];
           unsigned long long a2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            tmem_ld32(tl + half * 32, v);
+          for (int qc = 0; qc < 4; ++qc) {
+            tmem_ld16(tl + qc * 16, v);
             tmem_ld_wait_regs(v);
-            if (jj == C::QSW - 1 && half == 1) {
+            if (jj == C::QSW - 1 && qc == 3) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&ms->tm_empty[buf]);  // accumulators are in registers
             }
 #pragma unroll
-            for (int h4 = 0; h4 < 8; ++h4) {
-              const float4 ww = w4[half * 8 + h4];
+            for (int h4 = 0; h4 < 4; ++h4) {
+              const float4 ww = w4[qc * 4 + h4];
               const int b = (h4 & 1) * 2;
               a2[b + 0] = ffma2(ww.x, ww.y, fmaxf(v[4 * h4 + 0], 0.f), fmaxf(v[4 * h4 + 1], 0.f), a2[b + 0]);
               a2[b + 1] = ffma2(ww.z, ww.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f), a2[b + 1]);
