@@ -73,26 +73,43 @@ dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_
       qres != cudaDriverEntryPointSuccess || !fn)
     return DSA_ERR_CUDA;
 
-  // RoPE table: angle pos * theta^(-2i/128) in double, cos/sin rounded once to fp32
-  const size_t n = static_cast<size_t>(max_pos) * 64;
-  std::vector<float2> tab(n);
+  // RoPE table: angle pos * theta^(-2i/128) in double, cos/sin rounded once
+  // to fp32, stored lane-interleaved for the store kernel: float4 8v + j of a
+  // row holds pairs 8j + 2v and 8j + 2v + 1
+  const size_t n = static_cast<size_t>(max_pos) * 32;
+  std::vector<float4> tab(n);
   double freq[64];
   for (int i = 0; i < 64; ++i) freq[i] = std::pow(static_cast<double>(rope_theta), -(2.0 * i) / 128.0);
-  for (int32_t p = 0; p < max_pos; ++p)
+  for (int32_t p = 0; p < max_pos; ++p) {
+    float cs[128];
     for (int i = 0; i < 64; ++i) {
       const double a = static_cast<double>(p) * freq[i];
-      tab[static_cast<size_t>(p) * 64 + i] =
-          make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+      cs[2 * i] = static_cast<float>(std::cos(a));
+      cs[2 * i + 1] = static_cast<float>(std::sin(a));
     }
-  float g[128];
+    for (int j = 0; j < 8; ++j)
+      for (int v = 0; v < 4; ++v) {
+        const float* q = cs + 2 * (8 * j + 2 * v);
+        tab[static_cast<size_t>(p) * 32 + 8 * v + j] = make_float4(q[0], q[1], q[2], q[3]);
+      }
+  }
+  // gamma (fp32), interleaved the same way: float4 l holds dims 8l..8l+3 and
+  // float4 16 + l dims 8l+4..8l+7
+  float gl[128];
   for (int d = 0; d < 128; ++d) {
     if (gamma_bf16) {
       const uint32_t b = static_cast<uint32_t>(gamma_bf16[d]) << 16;
-      std::memcpy(&g[d], &b, 4);
+      std::memcpy(&gl[d], &b, 4);
     } else {
-      g[d] = 1.0f;
+      gl[d] = 1.0f;
     }
   }
+  float g[128];
+  for (int l = 0; l < 16; ++l)
+    for (int e = 0; e < 4; ++e) {
+      g[4 * l + e] = gl[8 * l + e];
+      g[64 + 4 * l + e] = gl[8 * l + 4 + e];
+    }
 
   dsa_ctx* c = new (std::nothrow) dsa_ctx();
   if (!c) return DSA_ERR_CUDA;
@@ -102,10 +119,10 @@ dsa_status dsa_ctx_create(dsa_ctx** out, float rope_theta, float rms_eps, int32_
   c->eps = rms_eps;
   c->max_pos = max_pos;
   c->encode_tiled = fn;
-  bool okk = cudaMalloc(&c->rope, n * sizeof(float2)) == cudaSuccess &&
+  bool okk = cudaMalloc(&c->rope, n * sizeof(float4)) == cudaSuccess &&
              cudaMalloc(&c->gamma, 128 * sizeof(float)) == cudaSuccess &&
              cudaMalloc(&c->status, sizeof(unsigned int)) == cudaSuccess &&
-             cudaMemcpy(c->rope, tab.data(), n * sizeof(float2), cudaMemcpyHostToDevice) == cudaSuccess &&
+             cudaMemcpy(c->rope, tab.data(), n * sizeof(float4), cudaMemcpyHostToDevice) == cudaSuccess &&
              cudaMemcpy(c->gamma, g, sizeof(g), cudaMemcpyHostToDevice) == cudaSuccess &&
              cudaMemset(c->status, 0, sizeof(unsigned int)) == cudaSuccess;
   if (!okk) {

@@ -23,7 +23,9 @@ struct dsa_ctx {
   float theta;
   float eps;
   int max_pos;
-  float2* rope;          // [max_pos][64] (cos, sin), fp32
+  // RoPE (cos, sin) in fp32, [max_pos][32] float4, lane-interleaved: float4
+  // 8v + j of a row holds pairs 8j + 2v and 8j + 2v + 1 (j < 8, v < 4)
+  float4* rope;
   int hadamard;          // store keys rotated by the 128-point Walsh-Hadamard transform
   int slot_output;       // top-k returns cache slots instead of positions
   float* gamma;          // [128]

@@ -18,6 +18,14 @@
 // shuffle. Every fp32 step uses the round-to-nearest intrinsics so no
 // multiply-add is contracted.
 //
+// The kernel is bound by the L1 data pipe (wavefronts), so the context keeps
+// its RoPE table and gamma in lane-interleaved layouts: lane j = l & 7 needs
+// the (cos, sin) pairs 8j..8j+7 of its position, as four 16-byte chunks,
+// and chunk v of every lane sits in one contiguous 128-byte block of the
+// row (float4 8v + j), so each of the four loads touches one line per token
+// instead of four; gamma's two float4 per lane are stored as [16 first
+// halves][16 second halves] likewise. Values and arithmetic are unchanged.
+//
 // Optional Hadamard rotation (same pages: the fused kernel applies a Hadamard
 // transform before the store): the unnormalised 128-point Walsh-Hadamard
 // transform in natural order, as butterflies h = 1, 2, 4 inside a lane's 8
@@ -42,7 +50,7 @@ template <int FMT, bool HAD>
 __global__ void __launch_bounds__(256) store_kernel(
     const uint4* __restrict__ k_raw, const int32_t* __restrict__ rope_pos,
     const int32_t* __restrict__ seq_id, const int32_t* __restrict__ page_table, int T, int B,
-    int max_pages, uint8_t* __restrict__ cache, int num_pages, const float2* __restrict__ rope,
+    int max_pages, uint8_t* __restrict__ cache, int num_pages, const float4* __restrict__ rope,
     int max_pos, const float* __restrict__ gamma, float eps, unsigned int* status) {
   pdl_wait();
   pdl_trigger();
@@ -66,8 +74,8 @@ __global__ void __launch_bounds__(256) store_kernel(
     pos = rope_pos[tok];
     s = seq_id[tok];
   }
-  g0 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * l);
-  g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 2 * l + 1);
+  g0 = __ldg(reinterpret_cast<const float4*>(gamma) + l);
+  g1 = __ldg(reinterpret_cast<const float4*>(gamma) + 16 + l);
   if (live) {
     ok = s >= 0 && s < B && pos >= 0 && pos < max_pos && pos < max_pages * kPage;
     if (ok) {
@@ -77,11 +85,10 @@ __global__ void __launch_bounds__(256) store_kernel(
     if (!ok && l == 0) atomicOr(status, DSA_DEV_BOUNDS);
   }
   const bool pos_ok = live && pos >= 0 && pos < max_pos;  // the RoPE row may be read
-  const float4* cs4 =
-      reinterpret_cast<const float4*>(rope + static_cast<long long>(pos_ok ? pos : 0) * 64 + 8 * (l & 7));
+  const float4* cs4 = rope + static_cast<long long>(pos_ok ? pos : 0) * 32 + (l & 7);
   float4 cst[4];
 #pragma unroll
-  for (int v = 0; v < 4; ++v) cst[v] = __ldg(cs4 + v);
+  for (int v = 0; v < 4; ++v) cst[v] = __ldg(cs4 + 8 * v);
 
   float x[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
                 bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
@@ -216,7 +223,7 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
   const cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, stream,
                                    static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B,
                                    max_pages, static_cast<uint8_t*>(cache), num_pages,
-                                   static_cast<const float2*>(ctx->rope), ctx->max_pos,
+                                   ctx->rope, ctx->max_pos,
                                    static_cast<const float*>(ctx->gamma), ctx->eps, ctx->status);
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -95,3 +95,49 @@ def test_store_rejects_bad_page_on_device(ctx):
     S.store(want, 0, wl.new_k[:64], wl.new_pos[:64], wl.new_seq[:64], wl.page_table, wl.num_pages)
     assert np.array_equal(U.slot_bytes(got, 0, wl, wl.new_pos[:64], wl.new_seq[:64]),
                           U.slot_bytes(want, 0, wl, wl.new_pos[:64], wl.new_seq[:64]))
+
+
+def _pipeline_tokens():
+    # the store runs a persistent grid of 4 CTAs x 16 half-warps per SM, each
+    # half-warp walking tokens g, g + G, ...: three grid strides and a ragged
+    # tail give every half-warp three or four tokens, and in the warps that
+    # straddle the tail the two halves different counts
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 3 * 16 * 4 * sms + 37
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
+def test_store_bitexact_several_tokens_per_half_warp(ctx, fmt):
+    T = _pipeline_tokens()
+    lens = [T // 3 + 5, T // 3 - 11, T - 2 * (T // 3) + 6]
+    wl = I.make_workload("pl", lens, [1] * 3, lens, True, 512, seed=24, wid=23)
+    assert wl.new_pos.shape[0] == T
+    d = U.device_workload(wl, fmt, ctx, store_fill=False)
+    assert ctx.device_status() == 0
+    _compare_cache(wl, fmt, d, wl.new_pos, wl.new_seq)
+
+
+def test_store_bad_pages_inside_a_long_run(ctx):
+    # two pages in the middle of a multi-token run point past the cache: those
+    # 128 tokens are dropped and reported, every other token is stored exactly
+    import torch
+    T = _pipeline_tokens()
+    wl = I.make_workload("pb", [T], [1], [T], True, 512, seed=25, wid=24)
+    bad_pages = [7, wl.page_table.shape[1] // 2]
+    for pg in bad_pages:
+        wl.page_table[0, pg] = wl.num_pages + pg
+    d = U.device_workload(wl, 0, ctx, store_fill=False, store_new=False)
+    k = U.t_bf16(wl.new_k).cuda()
+    pos = torch.from_numpy(wl.new_pos).cuda()
+    seq = torch.from_numpy(wl.new_seq).cuda()
+    ctx.store(k, pos, seq, d["page_table"], d["cache"], wl.num_pages, 0)
+    assert ctx.device_status() == 4          # DSA_ERR_DEVICE_BOUNDS
+    assert ctx.device_status() == 0
+    keep = ~np.isin(wl.new_pos // 64, bad_pages)
+    assert keep.sum() == T - 128
+    got = d["cache"].cpu().numpy()
+    want = S.new_cache(wl.num_pages, 0)
+    S.store(want, 0, wl.new_k[keep], wl.new_pos[keep], wl.new_seq[keep], wl.page_table, wl.num_pages)
+    assert np.array_equal(U.slot_bytes(got, 0, wl, wl.new_pos[keep], wl.new_seq[keep]),
+                          U.slot_bytes(want, 0, wl, wl.new_pos[keep], wl.new_seq[keep]))
