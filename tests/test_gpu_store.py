@@ -98,17 +98,16 @@ def test_store_rejects_bad_page_on_device(ctx):
 
 
 def _pipeline_tokens():
-    # the store runs a persistent grid of 4 CTAs x 16 half-warps per SM, each
-    # half-warp walking tokens g, g + G, ...: three grid strides and a ragged
-    # tail give every half-warp three or four tokens, and in the warps that
-    # straddle the tail the two halves different counts
+    # several waves of store CTAs (16 tokens each, up to 5 resident per SM)
+    # and a ragged tail: 3 x 64 tokens per SM plus 37, so the last CTA holds
+    # a partial token set and its second warp straddles the end of the batch
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return 3 * 16 * 4 * sms + 37
 
 
 @pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8, S.FMT_FP4])
-def test_store_bitexact_several_tokens_per_half_warp(ctx, fmt):
+def test_store_bitexact_several_waves(ctx, fmt):
     T = _pipeline_tokens()
     lens = [T // 3 + 5, T // 3 - 11, T - 2 * (T // 3) + 6]
     wl = I.make_workload("pl", lens, [1] * 3, lens, True, 512, seed=24, wid=23)
