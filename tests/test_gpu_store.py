@@ -99,8 +99,8 @@ def test_store_rejects_bad_page_on_device(ctx):
 
 def _pipeline_tokens():
     # several waves of store CTAs (16 tokens each, up to 5 resident per SM)
-    # and a ragged tail: 3 x 64 tokens per SM plus 37, so the last CTA holds
-    # a partial token set and its second warp straddles the end of the batch
+    # and a ragged tail: 3 x 64 tokens per SM plus 37 (the last CTA holds
+    # five tokens on a 152-SM part, and one of its warps straddles the end)
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return 3 * 16 * 4 * sms + 37
