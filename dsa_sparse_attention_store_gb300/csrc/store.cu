@@ -47,7 +47,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int FMT, bool HAD>
-__global__ void __launch_bounds__(256) store_kernel(
+__global__ void __launch_bounds__(128) store_kernel(
     const uint4* __restrict__ k_raw, const int32_t* __restrict__ rope_pos,
     const int32_t* __restrict__ seq_id, const int32_t* __restrict__ page_table, int T, int B,
     int max_pages, uint8_t* __restrict__ cache, int num_pages, const float4* __restrict__ rope,
@@ -215,12 +215,14 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
                         void* cache, int32_t num_pages, dsa_fmt fmt, cudaStream_t stream) {
   if (T == 0) return DSA_OK;
   const long long threads = static_cast<long long>(T) * 16;
-  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  // 128-thread blocks (8 tokens): 4 % faster than 256 on the 1.05M-token fill,
+  // 512 were 23 % slower
+  const unsigned blocks = static_cast<unsigned>((threads + 127) / 128);
   LaunchScope scope(ctx, DSA_K_STORE, stream);
   auto kern = fmt == DSA_FMT_BF16 ? (ctx->hadamard ? store_kernel<DSA_FMT_BF16, true> : store_kernel<DSA_FMT_BF16, false>)
                : fmt == DSA_FMT_FP8 ? (ctx->hadamard ? store_kernel<DSA_FMT_FP8, true> : store_kernel<DSA_FMT_FP8, false>)
                                     : (ctx->hadamard ? store_kernel<DSA_FMT_FP4, true> : store_kernel<DSA_FMT_FP4, false>);
-  const cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(256), 0, stream,
+  const cudaError_t e = launch_pdl(kern, dim3(blocks), dim3(128), 0, stream,
                                    static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B,
                                    max_pages, static_cast<uint8_t*>(cache), num_pages,
                                    ctx->rope, ctx->max_pos,
