@@ -18,8 +18,9 @@
 // shuffle. Every fp32 step uses the round-to-nearest intrinsics so no
 // multiply-add is contracted.
 //
-// The kernel is bound by the L1 data pipe (wavefronts), so the context keeps
-// its RoPE table and gamma in lane-interleaved layouts: lane j = l & 7 needs
+// Strided RoPE loads made the kernel bound by the L1 data pipe (wavefronts),
+// so the context keeps its RoPE table and gamma in lane-interleaved layouts
+// (after which the dependent load latency bounds it): lane j = l & 7 needs
 // the (cos, sin) pairs 8j..8j+7 of its position, as four 16-byte chunks,
 // and chunk v of every lane sits in one contiguous 128-byte block of the
 // row (float4 8v + j), so each of the four loads touches one line per token
@@ -46,15 +47,24 @@ constexpr int kPage = 64;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// The kernel is latency-bound (two dependent rounds of loads per token), so
+// it is compiled for 12 resident CTAs per SM (96 tokens in flight; 40
+// registers, with 16-24 bytes per thread spilled to L1): 6 % faster on the
+// 1.05M-token fill than the 10 CTAs its 47 registers allowed, in both
+// formats; 16 CTAs (32 registers) were 27 % slower.
 template <int FMT, bool HAD>
-__global__ void __launch_bounds__(128) store_kernel(
+__global__ void __launch_bounds__(128, 12) store_kernel(
     const uint4* __restrict__ k_raw, const int32_t* __restrict__ rope_pos,
     const int32_t* __restrict__ seq_id, const int32_t* __restrict__ page_table, int T, int B,
     int max_pages, uint8_t* __restrict__ cache, int num_pages, const float4* __restrict__ rope,
-    int max_pos, const float* __restrict__ gamma, float eps, unsigned int* status) {
+    int max_pos, const float* __restrict__ gamma, float eps, unsigned int* status, int R, int Cr) {
   pdl_wait();
   pdl_trigger();
-  const int tok = (blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  // chunk of 8 tokens: CTA b takes chunk j = b / R of region r = b % R, the
+  // token array being cut into R regions of Cr chunks
+  const long long chunk = static_cast<long long>(blockIdx.x % R) * Cr + blockIdx.x / R;
+  const long long tok_l = chunk * 8 + (threadIdx.x >> 4);
+  const int tok = tok_l < T ? static_cast<int>(tok_l) : T;
   const int l = threadIdx.x & 15;
   const bool live = tok < T;
 
@@ -214,10 +224,19 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
                         const int32_t* page_table, int32_t T, int32_t B, int32_t max_pages,
                         void* cache, int32_t num_pages, dsa_fmt fmt, cudaStream_t stream) {
   if (T == 0) return DSA_OK;
-  const long long threads = static_cast<long long>(T) * 16;
   // 128-thread blocks (8 tokens): 4 % faster than 256 on the 1.05M-token fill,
   // 512 were 23 % slower
-  const unsigned blocks = static_cast<unsigned>((threads + 127) / 128);
+  const long long chunks = (static_cast<long long>(T) + 7) / 8;
+  // The CTAs visit the token array in R interleaved regions (consecutive
+  // CTAs take the same chunk index of different regions). A batch of R (or a
+  // multiple of R) equal-length sequences stored one after another then has
+  // its R tokens of one position in flight together, so their shared RoPE
+  // table row comes from DRAM once instead of once per sequence; for any
+  // other layout the order is immaterial. Each region is still a contiguous
+  // stream of 2 KB chunks.
+  const int R = B >= 8 ? 8 : (B >= 1 ? B : 1);
+  const long long Cr = (chunks + R - 1) / R;
+  const unsigned blocks = static_cast<unsigned>(Cr * R);
   LaunchScope scope(ctx, DSA_K_STORE, stream);
   auto kern = fmt == DSA_FMT_BF16 ? (ctx->hadamard ? store_kernel<DSA_FMT_BF16, true> : store_kernel<DSA_FMT_BF16, false>)
                : fmt == DSA_FMT_FP8 ? (ctx->hadamard ? store_kernel<DSA_FMT_FP8, true> : store_kernel<DSA_FMT_FP8, false>)
@@ -226,7 +245,8 @@ dsa_status launch_store(dsa_ctx* ctx, const void* k_raw, const int32_t* pos, con
                                    static_cast<const uint4*>(k_raw), pos, seq, page_table, T, B,
                                    max_pages, static_cast<uint8_t*>(cache), num_pages,
                                    ctx->rope, ctx->max_pos,
-                                   static_cast<const float*>(ctx->gamma), ctx->eps, ctx->status);
+                                   static_cast<const float*>(ctx->gamma), ctx->eps, ctx->status, R,
+                                   static_cast<int>(Cr));
   return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -99,8 +99,10 @@ def test_store_rejects_bad_page_on_device(ctx):
 
 def _pipeline_tokens():
     # several waves of store CTAs (8 tokens each) and a ragged tail: 3 x 64
-    # tokens per SM plus 37 (the last CTA holds five tokens on a 152-SM part,
-    # and one of its warps straddles the end of the batch)
+    # tokens per SM plus 37 (the last 8-token chunk holds five tokens on a
+    # 152-SM part, and one warp of its CTA straddles the end of the batch;
+    # with 3 sequences the CTAs visit the chunks in 3 interleaved regions,
+    # and the last region has one chunk past the end)
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return 3 * 16 * 4 * sms + 37
