@@ -421,6 +421,8 @@ def measure_workload(name, args, ctx, dev, world, barrier, flush, peaks, peak_sr
             f"score_kernel ({FMT_NAMES[f]} cache)", sc_ms / max(sc_n, 1), nbytes, flops, f, peaks, peak_src,
             traffic_of(f"{name}/score/{FMT_NAMES[f]}", scorer_hash()), sc_n)
     out["roofline"] = roofs
+    if getattr(wl, "needles", None):
+        out["needle_report"] = needle_report(wl, dv, fmts, ctx, dev)
     if e2e_ms is not None:
         out["e2e"] = {"value": whole_job_rate(ks_step, args.steps, world, e2e_ms), "unit": "key-scores/s",
                       "h2d_bytes_per_step": dv.h2d_bytes(), "d2h_bytes_per_step": dv.d2h_bytes(),
@@ -428,6 +430,37 @@ def measure_workload(name, args, ctx, dev, world, barrier, flush, peaks, peak_sr
     if not args.no_fp4:
         out["fp4"] = measure_fp4(wl, name, args, ctx, dev, world, barrier, flush, peaks, peak_src)
     return out, wl, fmts, dv
+
+
+def needles_selected(wl, out_idx):
+    """How many needle queries selected each planted needle, from the GPU's
+    own output rows (the parity tests compare those rows with the oracle)."""
+    import numpy as np
+    sel = np.asarray(out_idx)[np.asarray(wl.needle_queries)]
+    per = [int((sel == p).any(axis=1).sum()) for p in wl.needles]
+    return {"selected_per_needle": per, "selected": sum(per), "of": len(wl.needle_queries) * len(wl.needles)}
+
+
+def needle_report(wl, dv, fmts, ctx, dev):
+    """Whether each needle is selected: for the timed workload (head weights
+    |N(0,1)|/8) from the last timed step's output, and for the same queries
+    and keys with signed weights N(0,1)/8 from one untimed call per format."""
+    import torch
+    from synth import inputs as I
+    rep = {"needle_positions": list(wl.needles), "needle_queries": len(wl.needle_queries),
+           "abs_weights": {FMT_NAMES[f]: needles_selected(wl, dv.outs[f][0].cpu().numpy()) for f in fmts}}
+    w = torch.from_numpy(I.needle(w_abs=False).head_w).to(dev)
+    signed = {}
+    for f in fmts:
+        oi, os_ = torch.empty_like(dv.outs[f][0]), torch.empty_like(dv.outs[f][1])
+        ctx.topk(dv.d["q"], w, dv.caches[f], wl.num_pages, f, dv.d["page_table"], dv.d["seq_lens"],
+                 dv.d["cu_q"], wl.causal, wl.k, oi, os_, dv.wss[f])
+        signed[FMT_NAMES[f]] = needles_selected(wl, oi.cpu().numpy())
+    rep["signed_weights"] = signed
+    st = ctx.device_status()
+    if st != 0:
+        raise RuntimeError(f"needle report: device status {st}")
+    return rep
 
 
 def measure_fp4(wl, name, args, ctx, dev, world, barrier, flush, peaks, peak_src):
@@ -723,6 +756,8 @@ def compose(args, world, results, stores, wls, clocks):
     }
     if "e2e" in h:
         out["e2e"] = h["e2e"]
+    if "needle_report" in h:
+        out["needle_report"] = h["needle_report"]
     if stores:
         out["store_roofline"] = stores
     out["configs"] = {n: r for n, r in results.items() if n != head}

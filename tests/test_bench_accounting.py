@@ -45,3 +45,18 @@ def test_whole_job_rate_weak_scaling():
     b = _bench()
     assert b.whole_job_rate(1000, 10, 1, 5.0) == 1000 * 10 / 0.005
     assert b.whole_job_rate(1000, 10, 4, 5.0) == 4 * b.whole_job_rate(1000, 10, 1, 5.0)
+
+
+def test_needles_selected_counts_each_needle_per_query():
+    # three needle queries (rows 1, 2, 3 of four) and two needles at
+    # positions 10 and 20: row 1 selected both, row 2 only the first, row 3
+    # neither; row 0 is not a needle query and is ignored
+    b = _bench()
+
+    class W:
+        needle_queries = (1, 2, 3)
+        needles = (10, 20)
+
+    out = np.array([[10, 20, 30], [20, 5, 10], [10, 7, -1], [1, 2, 3]], dtype=np.int32)
+    rep = b.needles_selected(W(), out)
+    assert rep == {"selected_per_needle": [2, 1], "selected": 3, "of": 6}

@@ -129,6 +129,26 @@ def test_needle_config(ctx, fmt):
             assert p in sel, f"needle at {p} missing for query {r}"
 
 
+@functools.lru_cache(maxsize=None)
+def _signed_needle():
+    return I.needle(w_abs=False)
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_BF16, S.FMT_FP8])
+def test_needle_signed_weights(ctx, fmt, record_property):
+    # the needle workload with signed head weights N(0,1)/8: every row
+    # against the oracle; with signed weights a needle need not score
+    # highest, so how many needle queries select each needle is only
+    # reported (the set match above already fixes it to the oracle's)
+    wl = _signed_needle()
+    gi, _, summ = _check(wl, fmt, ctx)
+    assert summ["rows"] == wl.Tq
+    sel = gi[np.asarray(wl.needle_queries)]
+    per = [int((sel == p).any(axis=1).sum()) for p in wl.needles]
+    record_property("needles_selected_per_depth", per)
+    print(f"signed weights, fmt {fmt}: needle queries selecting each needle {per} of {len(wl.needle_queries)}")
+
+
 @pytest.mark.parametrize("fmt", FMTS)
 def test_long_prefill_config(ctx, fmt):
     # the 22528-token causal prefill, every row against the C++ oracle; the
